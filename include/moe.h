@@ -1,0 +1,173 @@
+/*
+ * moe.h -- C ABI of the int4 routed-expert MoE block for GB300 (sm_103a).
+ *
+ * The block is the sparse Mixture-of-Experts layer of the Qwen3-Next /
+ * Qwen3.5-3.6 hybrid decoders described in the Swiftlet project README
+ * ("Show HN: Run an 80B Qwen in 4.3 GB of RAM on a Mac and a 35B on an
+ * iPhone", wpnews), section "How it works": each layer routes every token to
+ * k of E experts (8 of 256 for Qwen3.6-35B-A3B, 10 of 512 for
+ * Qwen3-Next-80B-A3B), keeps a shared expert resident, and stores the experts
+ * in MLX affine int4 group quantisation (same README, list of what was built:
+ * "MLX affine int4/int8 group quantization", "byte-addressed kernels with
+ * 64-bit offsets for multi-gigabyte shards").  For every token t:
+ *
+ *   l[t,e]  = x_t . Wr_e (+ prior_e)                        router
+ *   idx, w  = top-k of softmax(l[t,:]) (descending, ties -> lowest e),
+ *             renormalised to sum to one                     routing
+ *   p       = t*k + j, stable counting sort by idx[t,j]      permutation
+ *   o[t,j]  = Wd (silu(Wg x_t) * (Wu x_t)), W = s*q + b      routed experts
+ *   y_t     = sum_j w[t,j] o[t,j] + sigmoid(x_t . wsg) S(x_t)  combine
+ *
+ * where S is the shared expert (same form, inner size shared_inter) and the
+ * int4 codes q are grouped in `group` consecutive inputs sharing one bf16
+ * scale s and bias b.  Expert selection ranks the exact real values of the
+ * logits (bf16 x bf16 products summed without rounding), so the selected
+ * indices do not depend on any summation order.
+ *
+ * Conventions
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Packed int4: code 8c+j of a row is bits 4j..4j+3 of uint32 word c.
+ *   - Every function returns a moe_status (0 = MOE_OK, negative = error);
+ *     moe_last_error(ctx) gives a one-line message.  Nothing here throws,
+ *     aborts or prints.
+ *   - A context is bound to the CUDA device that is current at moe_create;
+ *     all later calls must be made with that device current.
+ *   - Device pointers are plain CUDA device addresses; `stream` is a
+ *     cudaStream_t (NULL = legacy default stream).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* a size, pointer or option is out of range       */
+  MOE_ERR_CUDA = -2,         /* a CUDA runtime call failed (message has details)  */
+  MOE_ERR_OOM = -3,          /* device memory could not be allocated             */
+  MOE_ERR_NOT_LOADED = -4,   /* moe_forward before moe_load_weights              */
+  MOE_ERR_NOT_RESERVED = -5, /* moe_forward before moe_reserve, or T > max_T     */
+  MOE_ERR_SLOT = -6,         /* device: a selected expert maps to no valid slot  */
+  MOE_ERR_TIMEOUT = -7,      /* device: a bounded wait inside a kernel expired   */
+  MOE_ERR_UNSUPPORTED = -8   /* sizes outside what the kernels were built for    */
+} moe_status;
+
+typedef struct moe_ctx moe_ctx;
+
+/* One int4 matrix [rows][cols] in MLX affine layout:
+ *   q  uint32 [rows][cols/8]      packed codes
+ *   s  bf16   [rows][cols/group]  scales
+ *   b  bf16   [rows][cols/group]  biases            w = s*q + b
+ * For a stack of matrices the arrays carry one more leading dimension. */
+typedef struct moe_qmatrix {
+  const uint32_t* q;
+  const uint16_t* s;
+  const uint16_t* b;
+} moe_qmatrix;
+
+/* Canonical weights of one MoE layer.  With on_device = 1 every pointer is a
+ * device address, with 0 a host address.  E, H = hidden, I = inter,
+ * Is = shared_inter, n = n_slots.
+ *   router_w       bf16 [E][H]
+ *   router_bias    fp32 [E], or NULL (no additive prior on the logits)
+ *   shared_gate_w  bf16 [H]   (sigmoid gate of the shared expert)
+ *   shared_gate, shared_up   [Is][H] int4 (leading dim 1 allowed, ignored)
+ *   shared_down              [H][Is] int4
+ *   gate, up                 [n][I][H] int4, slot-major
+ *   down                     [n][H][I] int4, slot-major                    */
+typedef struct moe_weights {
+  int on_device;
+  const uint16_t* router_w;
+  const float* router_bias;
+  const uint16_t* shared_gate_w;
+  moe_qmatrix shared_gate, shared_up, shared_down;
+  moe_qmatrix gate, up, down;
+} moe_weights;
+
+/* Create a context for one MoE layer.
+ *   E in [1, 1024]; k in [1, min(E, 32)]; hidden a multiple of 256, at most
+ *   8192; inter and shared_inter multiples of group, at most 4096; group in
+ *   {32, 64, 128}.  Nothing is allocated on the device yet.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for sizes out of range,
+ * MOE_ERR_CUDA if no device is current. */
+int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out);
+
+/* Copy and repack the weights into library-owned device memory: the routed
+ * experts become n_slots fixed-stride blobs (slot s holds the s-th expert of
+ * `w`, 64-bit byte offsets), the router, prior, shared gate vector and shared
+ * expert stay resident beside them.  Synchronous: when it returns the caller
+ * may free or reuse every buffer of `w`.  May be called again to replace the
+ * weights (the previous ones are freed).  n_slots in [1, 65536].
+ * Errors: INVALID_ARG (null pointers, n_slots), OOM, CUDA. */
+int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stream);
+
+/* Size the device workspace for up to max_T tokens per moe_forward call
+ * (max_T in [1, 1<<20]).  Must be called before moe_forward and before any
+ * CUDA-graph capture of it; moe_forward never allocates.  Synchronous.
+ * Errors: INVALID_ARG, OOM. */
+int moe_reserve(moe_ctx* ctx, int max_T);
+
+/* One pass of the block over T tokens, enqueued on `stream` (asynchronous,
+ * no host synchronisation, no allocation: capturable in a CUDA graph).
+ *   x                  bf16 [T][H] device, read only
+ *   expert_slot_table  int32 [E] device: slot holding expert e, or NULL for
+ *                      the identity (requires n_slots >= E).  A selected
+ *                      expert whose slot is negative or >= n_slots makes the
+ *                      device record MOE_ERR_SLOT and skip that expert.
+ *   y                  bf16 [T][H] device, written
+ *   topk_idx           int32 [T][k] device, written: expert ids, descending
+ *                      exact logit, ties to the lowest id
+ *   topk_w             fp32 [T][k] device, written: renormalised weights
+ *   perm               int32 [T*k] device or NULL: pair ids p = t*k+j sorted
+ *                      stably by expert
+ *   offsets            int32 [E+1] device or NULL: expert e's pairs are
+ *                      perm[offsets[e] .. offsets[e+1])
+ * T = 0 is a no-op.  x and y must not overlap.
+ * Errors (host side, nothing launched): INVALID_ARG, NOT_LOADED,
+ * NOT_RESERVED (T > max_T), CUDA (launch failure).  Errors found on the
+ * device are sticky and reported by moe_get_status. */
+int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_table, void* y,
+                int32_t* topk_idx, float* topk_w, int32_t* perm, int32_t* offsets, void* stream);
+
+/* Synchronise `stream`, then return and clear the sticky device error word
+ * (MOE_OK, MOE_ERR_SLOT or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the
+ * synchronisation itself failed. */
+int moe_get_status(moe_ctx* ctx, void* stream);
+
+/* Read slot `slot` (or the shared expert when slot == -1) back from the
+ * device pool into host buffers in the canonical layout of moe_weights
+ * (gate/up [I][H], down [H][I]; I = shared_inter for the shared expert).
+ * Synchronous.  Used to verify the repacking byte for byte. */
+int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, uint16_t* gate_b,
+                    uint32_t* up_q, uint16_t* up_s, uint16_t* up_b, uint32_t* down_q,
+                    uint16_t* down_s, uint16_t* down_b);
+
+/* Kernel path of moe_forward: MOE_PATH_AUTO picks by T (decode kernels up
+ * to 64 tokens, grouped GEMM above); the others force one path. */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_GENERAL = 2, MOE_PATH_PREFILL = 3 };
+int moe_set_path(moe_ctx* ctx, int path);
+
+/* Bytes of one routed-expert blob (codes + scales + biases, padded) and the
+ * number of resident device bytes of the context (weights + workspace). */
+int64_t moe_expert_blob_bytes(const moe_ctx* ctx);
+int64_t moe_device_bytes(const moe_ctx* ctx);
+
+/* Number of kernel launches the last moe_forward enqueued. */
+int moe_last_launch_count(const moe_ctx* ctx);
+
+const char* moe_last_error(const moe_ctx* ctx);
+const char* moe_status_string(int status);
+
+/* Free every device allocation of the context (synchronises the device
+ * first).  NULL is a no-op. */
+void moe_destroy(moe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,438 @@
+// api.cu -- the C ABI declared in include/moe.h: argument checks, device
+// memory, weight loading/repacking and the launch sequence of moe_forward.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_ctx {
+  Ctx c;
+};
+
+namespace {
+
+thread_local char g_create_msg[512];
+
+int set_msg(moe_ctx* ctx, int code, const char* fmt, ...) {
+  char* buf = ctx ? ctx->c.msg : g_create_msg;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, 512, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(moe_ctx* ctx, cudaError_t e, const char* what) {
+  const int code = (e == cudaErrorMemoryAllocation) ? MOE_ERR_OOM : MOE_ERR_CUDA;
+  return set_msg(ctx, code, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev && dev >= 0) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+template <typename T>
+void free_dev(T*& p) {
+  if (p) cudaFree(p);
+  p = nullptr;
+}
+
+void free_weights(Ctx& c) {
+  free_dev(c.router_w);
+  free_dev(c.router_bias);
+  free_dev(c.shared_gate_w);
+  free_dev(c.pool);
+  free_dev(c.shared);
+  c.n_slots = 0;
+  c.weight_bytes = 0;
+}
+
+void free_workspace(Ctx& c) {
+  if (c.ws_base) cudaFree(c.ws_base);
+  c.ws_base = nullptr;
+  c.ws_bytes = 0;
+  c.ws = Workspace{};
+  c.err = nullptr;
+  c.max_T = 0;
+}
+
+uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+
+bool qm_ok(const moe_qmatrix& m) { return m.q && m.s && m.b; }
+
+// Sizes in bytes of one canonical expert's nine arrays.
+struct CanonSizes {
+  size_t gq, gsb, dq, dsb;  // q words of gate (= up), s (= b) of gate, q of down, s of down
+};
+CanonSizes canon_sizes(int H, int I, int G) {
+  CanonSizes s;
+  s.gq = (size_t)I * (H / 8) * 4;
+  s.gsb = (size_t)I * (H / G) * 2;
+  s.dq = (size_t)H * (I / 8) * 4;
+  s.dsb = (size_t)H * (I / G) * 2;
+  return s;
+}
+
+// Copy `n` experts starting at index e0 of the canonical arrays (host or
+// device) into blobs[0..n), staging host data through device memory.
+int load_experts(moe_ctx* ctx, const moe_qmatrix& g, const moe_qmatrix& u, const moe_qmatrix& d,
+                 int e0, int n, int on_device, int H, int I, int G, uint8_t* blobs,
+                 const BlobLayout& L, cudaStream_t st) {
+  const CanonSizes cs = canon_sizes(H, I, G);
+  if (on_device) {
+    cudaError_t e = launch_repack_expert(
+        g.q + (size_t)e0 * cs.gq / 4, g.s + (size_t)e0 * cs.gsb / 2, g.b + (size_t)e0 * cs.gsb / 2,
+        u.q + (size_t)e0 * cs.gq / 4, u.s + (size_t)e0 * cs.gsb / 2, u.b + (size_t)e0 * cs.gsb / 2,
+        d.q + (size_t)e0 * cs.dq / 4, d.s + (size_t)e0 * cs.dsb / 2, d.b + (size_t)e0 * cs.dsb / 2,
+        n, H, I, G, blobs, L, st);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "repack");
+    return MOE_OK;
+  }
+  const size_t per = 2 * cs.gq + 4 * cs.gsb + cs.dq + 2 * cs.dsb;
+  const int chunk = (int)((256ull << 20) / per > 0 ? (256ull << 20) / per : 1);
+  uint8_t* stage = nullptr;
+  const int cap = chunk < n ? chunk : n;
+  cudaError_t e = cudaMalloc(&stage, per * (size_t)cap);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "staging allocation");
+  int rc = MOE_OK;
+  for (int s0 = 0; s0 < n && rc == MOE_OK; s0 += cap) {
+    const int m = (n - s0) < cap ? (n - s0) : cap;
+    const size_t E0 = (size_t)(e0 + s0);
+    uint8_t* p = stage;
+    auto put = [&](const void* src, size_t bytes_each) -> uint8_t* {
+      uint8_t* dst = p;
+      const size_t bytes = bytes_each * m;
+      if (cudaMemcpyAsync(dst, (const uint8_t*)src + E0 * bytes_each, bytes,
+                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+        rc = MOE_ERR_CUDA;
+      p += bytes;
+      return dst;
+    };
+    uint8_t* gq = put(g.q, cs.gq);
+    uint8_t* gs = put(g.s, cs.gsb);
+    uint8_t* gb = put(g.b, cs.gsb);
+    uint8_t* uq = put(u.q, cs.gq);
+    uint8_t* us = put(u.s, cs.gsb);
+    uint8_t* ub = put(u.b, cs.gsb);
+    uint8_t* dq = put(d.q, cs.dq);
+    uint8_t* ds = put(d.s, cs.dsb);
+    uint8_t* db = put(d.b, cs.dsb);
+    if (rc != MOE_OK) {
+      rc = set_msg(ctx, MOE_ERR_CUDA, "host-to-device copy of expert weights failed");
+      break;
+    }
+    e = launch_repack_expert((uint32_t*)gq, (uint16_t*)gs, (uint16_t*)gb, (uint32_t*)uq,
+                             (uint16_t*)us, (uint16_t*)ub, (uint32_t*)dq, (uint16_t*)ds,
+                             (uint16_t*)db, m, H, I, G, blobs + (size_t)s0 * L.stride, L, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) rc = cuda_fail(ctx, e, "repack");
+  }
+  cudaFree(stage);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_NOT_LOADED: return "weights not loaded";
+    case MOE_ERR_NOT_RESERVED: return "workspace not reserved for this many tokens";
+    case MOE_ERR_SLOT: return "a selected expert has no valid slot";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait expired";
+    case MOE_ERR_UNSUPPORTED: return "unsupported sizes";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error(const moe_ctx* ctx) { return ctx ? ctx->c.msg : g_create_msg; }
+
+int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out) {
+  if (!out) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (E < 1 || E > kMaxE) return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "E=%d not in [1, %d]", E, kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "k=%d not in [1, min(E, %d)]", k, kMaxK);
+  if (group != 32 && group != 64 && group != 128)
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "group=%d not in {32, 64, 128}", group);
+  if (hidden < 256 || hidden > kMaxH || hidden % 256 != 0)
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "hidden=%d must be a multiple of 256 in [256, %d]",
+                   hidden, kMaxH);
+  if (inter < group || inter > kMaxInter || inter % group != 0 || shared_inter < group ||
+      shared_inter > kMaxInter || shared_inter % group != 0)
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED,
+                   "inter=%d / shared_inter=%d must be multiples of group=%d in [group, %d]", inter,
+                   shared_inter, group, kMaxInter);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_msg(nullptr, MOE_ERR_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  moe_ctx* ctx = new (std::nothrow) moe_ctx();
+  if (!ctx) return set_msg(nullptr, MOE_ERR_OOM, "host allocation failed");
+  ctx->c.device = dev;
+  ctx->c.d = Dims{E, k, hidden, inter, shared_inter, group};
+  ctx->c.ex = make_blob_layout(hidden, inter, group);
+  ctx->c.sh = make_blob_layout(hidden, shared_inter, group);
+  *out = ctx;
+  return MOE_OK;
+}
+
+int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stream) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (!w) return set_msg(ctx, MOE_ERR_INVALID_ARG, "weights is NULL");
+  if (n_slots < 1 || n_slots > 65536)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "n_slots=%d not in [1, 65536]", n_slots);
+  if (!w->router_w || !w->shared_gate_w || !qm_ok(w->shared_gate) || !qm_ok(w->shared_up) ||
+      !qm_ok(w->shared_down) || !qm_ok(w->gate) || !qm_ok(w->up) || !qm_ok(w->down))
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "a weight pointer is NULL");
+  DeviceGuard guard(ctx->c.device);
+  Ctx& c = ctx->c;
+  const Dims& d = c.d;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaStreamSynchronize(st);
+  free_weights(c);
+  cudaError_t e;
+  const size_t rw_bytes = (size_t)d.E * d.H * 2;
+  if ((e = cudaMalloc(&c.router_w, rw_bytes)) != cudaSuccess) return cuda_fail(ctx, e, "router alloc");
+  if ((e = cudaMalloc(&c.shared_gate_w, (size_t)d.H * 2)) != cudaSuccess)
+    return cuda_fail(ctx, e, "shared gate alloc");
+  if (w->router_bias && (e = cudaMalloc(&c.router_bias, (size_t)d.E * 4)) != cudaSuccess)
+    return cuda_fail(ctx, e, "prior alloc");
+  if ((e = cudaMalloc(&c.pool, (size_t)n_slots * c.ex.stride)) != cudaSuccess) {
+    free_weights(c);
+    return cuda_fail(ctx, e, "expert pool alloc");
+  }
+  if ((e = cudaMalloc(&c.shared, c.sh.stride)) != cudaSuccess) {
+    free_weights(c);
+    return cuda_fail(ctx, e, "shared expert alloc");
+  }
+  const cudaMemcpyKind kind = w->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  e = cudaMemcpyAsync(c.router_w, w->router_w, rw_bytes, kind, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c.shared_gate_w, w->shared_gate_w, (size_t)d.H * 2, kind, st);
+  if (e == cudaSuccess && w->router_bias)
+    e = cudaMemcpyAsync(c.router_bias, w->router_bias, (size_t)d.E * 4, kind, st);
+  if (e != cudaSuccess) {
+    free_weights(c);
+    return cuda_fail(ctx, e, "router copy");
+  }
+  int rc = load_experts(ctx, w->gate, w->up, w->down, 0, n_slots, w->on_device, d.H, d.I, d.G,
+                        c.pool, c.ex, st);
+  if (rc == MOE_OK)
+    rc = load_experts(ctx, w->shared_gate, w->shared_up, w->shared_down, 0, 1, w->on_device, d.H,
+                      d.Is, d.G, c.shared, c.sh, st);
+  if (rc == MOE_OK && (e = cudaStreamSynchronize(st)) != cudaSuccess) rc = cuda_fail(ctx, e, "load");
+  if (rc != MOE_OK) {
+    free_weights(c);
+    return rc;
+  }
+  c.n_slots = n_slots;
+  c.weight_bytes = (int64_t)rw_bytes + d.H * 2 + (w->router_bias ? d.E * 4 : 0) +
+                   (int64_t)n_slots * c.ex.stride + (int64_t)c.sh.stride;
+  return MOE_OK;
+}
+
+int moe_reserve(moe_ctx* ctx, int max_T) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (max_T < 1 || max_T > (1 << 20))
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "max_T=%d not in [1, 2^20]", max_T);
+  DeviceGuard guard(ctx->c.device);
+  Ctx& c = ctx->c;
+  const Dims& d = c.d;
+  cudaDeviceSynchronize();
+  free_workspace(c);
+  const uint64_t P = (uint64_t)max_T * d.k;
+  const uint64_t rows = P + max_T;
+  const int maxI = d.I > d.Is ? d.I : d.Is;
+  const uint64_t nblk = (P + 2047) / 2048;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const uint64_t o_logits = take((uint64_t)max_T * d.E * 4);
+  const uint64_t o_bound = take((uint64_t)max_T * d.E * 4);
+  const uint64_t o_gz = take((uint64_t)max_T * 4);
+  const uint64_t o_gate = take((uint64_t)max_T * 4);
+  const uint64_t o_perm = take(P * 4);
+  const uint64_t o_inv = take(P * 4);
+  const uint64_t o_off = take((uint64_t)(d.E + 1) * 4);
+  const uint64_t o_used = take((uint64_t)d.E * 4);
+  const uint64_t o_nused = take(4);
+  const uint64_t o_hist = take(nblk * d.E * 4);
+  const uint64_t o_h = take(rows * maxI * 4);
+  const uint64_t o_o = take(rows * d.H * 4);
+  const uint64_t o_err = take(4);
+  uint8_t* base = nullptr;
+  cudaError_t e = cudaMalloc(&base, off);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace alloc");
+  e = cudaMemset(base, 0, off);
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    return cuda_fail(ctx, e, "workspace clear");
+  }
+  c.ws_base = base;
+  c.ws_bytes = (int64_t)off;
+  c.ws.logits = (float*)(base + o_logits);
+  c.ws.bound = (float*)(base + o_bound);
+  c.ws.gate_z = (float*)(base + o_gz);
+  c.ws.gate = (float*)(base + o_gate);
+  c.ws.perm = (int32_t*)(base + o_perm);
+  c.ws.inv = (int32_t*)(base + o_inv);
+  c.ws.offsets = (int32_t*)(base + o_off);
+  c.ws.used = (int32_t*)(base + o_used);
+  c.ws.n_used = (int32_t*)(base + o_nused);
+  c.ws.hist = (int32_t*)(base + o_hist);
+  c.ws.h = (float*)(base + o_h);
+  c.ws.o = (float*)(base + o_o);
+  c.err = (int32_t*)(base + o_err);
+  c.max_T = max_T;
+  if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess) {
+    free_workspace(c);
+    return cuda_fail(ctx, e, "kernel attributes");
+  }
+  return MOE_OK;
+}
+
+int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_table, void* y,
+                int32_t* topk_idx, float* topk_w, int32_t* perm, int32_t* offsets, void* stream) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  Ctx& c = ctx->c;
+  c.last_launches = 0;
+  if (T < 0) return set_msg(ctx, MOE_ERR_INVALID_ARG, "T=%d < 0", T);
+  if (T == 0) return MOE_OK;
+  if (!c.pool) return set_msg(ctx, MOE_ERR_NOT_LOADED, "moe_load_weights has not been called");
+  if (!c.ws_base) return set_msg(ctx, MOE_ERR_NOT_RESERVED, "moe_reserve has not been called");
+  if (T > c.max_T) return set_msg(ctx, MOE_ERR_NOT_RESERVED, "T=%d > reserved max_T=%d", T, c.max_T);
+  if (!x || !y || !topk_idx || !topk_w)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "x, y, topk_idx and topk_w must be non-NULL");
+  if (!expert_slot_table && c.n_slots < c.d.E)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG,
+                   "identity slot table needs n_slots (%d) >= E (%d)", c.n_slots, c.d.E);
+  if (((uintptr_t)x & 15) != 0)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  const size_t xb = (size_t)T * c.d.H * 2;
+  const uint8_t* xp = (const uint8_t*)x;
+  const uint8_t* yp = (const uint8_t*)y;
+  if (xp < yp + xb && yp < xp + xb) return set_msg(ctx, MOE_ERR_INVALID_ARG, "x and y overlap");
+  DeviceGuard guard(c.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  FwdArgs a{(const uint16_t*)x, T, expert_slot_table, (uint16_t*)y, topk_idx, topk_w, perm, offsets};
+  int launches = 0;
+  cudaError_t e = launch_router(c, a, st, &launches);
+  if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+  if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
+  if (e == cudaSuccess) e = launch_general_experts(c, a, st, &launches);
+  c.last_launches = launches;
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "moe_forward launch");
+  return MOE_OK;
+}
+
+int moe_get_status(moe_ctx* ctx, void* stream) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  DeviceGuard guard(ctx->c.device);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream synchronise");
+  if (!ctx->c.err) return MOE_OK;
+  int32_t v = 0;
+  e = cudaMemcpy(&v, ctx->c.err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+  if (v != 0) {
+    cudaMemset(ctx->c.err, 0, 4);
+    return set_msg(ctx, v, "device reported: %s", moe_status_string(v));
+  }
+  return MOE_OK;
+}
+
+int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, uint16_t* gate_b,
+                    uint32_t* up_q, uint16_t* up_s, uint16_t* up_b, uint32_t* down_q,
+                    uint16_t* down_s, uint16_t* down_b) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  Ctx& c = ctx->c;
+  if (!c.pool) return set_msg(ctx, MOE_ERR_NOT_LOADED, "no weights loaded");
+  if (slot < -1 || slot >= c.n_slots)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "slot=%d not in [-1, %d)", slot, c.n_slots);
+  if (!gate_q || !gate_s || !gate_b || !up_q || !up_s || !up_b || !down_q || !down_s || !down_b)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "an output pointer is NULL");
+  DeviceGuard guard(c.device);
+  const int I = slot < 0 ? c.d.Is : c.d.I;
+  const BlobLayout& L = slot < 0 ? c.sh : c.ex;
+  const uint8_t* blob = slot < 0 ? c.shared : c.pool + (uint64_t)slot * L.stride;
+  const CanonSizes cs = canon_sizes(c.d.H, I, c.d.G);
+  const size_t total = 2 * cs.gq + 4 * cs.gsb + cs.dq + 2 * cs.dsb;
+  uint8_t* stage = nullptr;
+  cudaError_t e = cudaMalloc(&stage, total);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "staging alloc");
+  uint8_t* p = stage;
+  uint8_t* dgq = p; p += cs.gq;
+  uint8_t* dgs = p; p += cs.gsb;
+  uint8_t* dgb = p; p += cs.gsb;
+  uint8_t* duq = p; p += cs.gq;
+  uint8_t* dus = p; p += cs.gsb;
+  uint8_t* dub = p; p += cs.gsb;
+  uint8_t* ddq = p; p += cs.dq;
+  uint8_t* dds = p; p += cs.dsb;
+  uint8_t* ddb = p;
+  e = launch_unpack_expert(blob, c.d.H, I, c.d.G, L, (uint32_t*)dgq, (uint16_t*)dgs,
+                           (uint16_t*)dgb, (uint32_t*)duq, (uint16_t*)dus, (uint16_t*)dub,
+                           (uint32_t*)ddq, (uint16_t*)dds, (uint16_t*)ddb, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  struct {
+    void* dst;
+    const void* src;
+    size_t n;
+  } cp[9] = {{gate_q, dgq, cs.gq}, {gate_s, dgs, cs.gsb}, {gate_b, dgb, cs.gsb},
+             {up_q, duq, cs.gq},   {up_s, dus, cs.gsb},   {up_b, dub, cs.gsb},
+             {down_q, ddq, cs.dq}, {down_s, dds, cs.dsb}, {down_b, ddb, cs.dsb}};
+  for (int i = 0; i < 9 && e == cudaSuccess; ++i)
+    e = cudaMemcpy(cp[i].dst, cp[i].src, cp[i].n, cudaMemcpyDeviceToHost);
+  cudaFree(stage);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "read back");
+  return MOE_OK;
+}
+
+int moe_set_path(moe_ctx* ctx, int path) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "path=%d unknown", path);
+  ctx->c.path = path;
+  return MOE_OK;
+}
+
+int64_t moe_expert_blob_bytes(const moe_ctx* ctx) { return ctx ? (int64_t)ctx->c.ex.stride : 0; }
+
+int64_t moe_device_bytes(const moe_ctx* ctx) {
+  return ctx ? ctx->c.weight_bytes + ctx->c.ws_bytes : 0;
+}
+
+int moe_last_launch_count(const moe_ctx* ctx) { return ctx ? ctx->c.last_launches : 0; }
+
+void moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return;
+  {
+    DeviceGuard guard(ctx->c.device);
+    cudaDeviceSynchronize();
+    free_weights(ctx->c);
+    free_workspace(ctx->c);
+  }
+  delete ctx;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// moe_internal.cuh -- shared declarations of the CUDA library (host + device).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kMaxH = 8192;
+constexpr int kMaxInter = 4096;
+constexpr int kDecodeMaxT = 64;
+
+// Byte offsets of the four regions of one expert blob.  Layout of a blob
+// (all words uint32, offsets 256-byte aligned, 64-bit throughout):
+//   gu_q  [I][2][H/8]   row 2i = gate row i, row 2i+1 = up row i (packed codes)
+//   gu_sb [I][2][H/G]   (bf16 scale) | (bf16 bias) << 16, same row order
+//   d_q   [H][I/8]      down rows
+//   d_sb  [H][I/G]
+struct BlobLayout {
+  uint64_t gu_q, gu_sb, d_q, d_sb, stride;
+};
+
+BlobLayout make_blob_layout(int H, int I, int G);
+
+struct Dims {
+  int E, k, H, I, Is, G;
+};
+
+// Workspace carved out of one allocation by moe_reserve.
+struct Workspace {
+  float* logits;      // [max_T][E]  fp32 router logits
+  float* bound;       // [max_T][E]  rigorous bound on their rounding error
+  float* gate_z;      // [max_T]     x . wsg (shared gate pre-activation)
+  float* gate;        // [max_T]     sigmoid(x . wsg)
+  int32_t* perm;      // [max_T*k]   pair ids sorted by expert
+  int32_t* inv;       // [max_T*k]   position of pair p in perm
+  int32_t* offsets;   // [E+1]
+  int32_t* used;      // [E]         experts with at least one pair, ascending
+  int32_t* n_used;    // [1]
+  int32_t* hist;      // [nblk][E]   per-block expert counts (large T)
+  float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
+  float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
+};
+
+struct Ctx {
+  int device = -1;
+  Dims d{};
+  int n_slots = 0;
+  int path = MOE_PATH_AUTO;
+  // resident weights
+  uint16_t* router_w = nullptr;       // [E][H]
+  float* router_bias = nullptr;       // [E] or null
+  uint16_t* shared_gate_w = nullptr;  // [H]
+  uint8_t* pool = nullptr;            // n_slots routed blobs
+  BlobLayout ex{};
+  uint8_t* shared = nullptr;          // one blob (inner size Is)
+  BlobLayout sh{};
+  int64_t weight_bytes = 0;
+  // workspace
+  int max_T = 0;
+  void* ws_base = nullptr;
+  int64_t ws_bytes = 0;
+  Workspace ws{};
+  int32_t* err = nullptr;             // sticky device error word
+  int last_launches = 0;
+  char msg[512] = {0};
+};
+
+// ---- kernels' host launchers (return cudaError_t of the last launch) ----
+cudaError_t launch_repack_expert(const uint32_t* gq, const uint16_t* gs, const uint16_t* gb,
+                                 const uint32_t* uq, const uint16_t* us, const uint16_t* ub,
+                                 const uint32_t* dq, const uint16_t* ds, const uint16_t* db,
+                                 int n, int H, int I, int G, uint8_t* blobs,
+                                 const BlobLayout& L, cudaStream_t st);
+cudaError_t launch_unpack_expert(const uint8_t* blob, int H, int I, int G, const BlobLayout& L,
+                                 uint32_t* gq, uint16_t* gs, uint16_t* gb, uint32_t* uq,
+                                 uint16_t* us, uint16_t* ub, uint32_t* dq, uint16_t* ds,
+                                 uint16_t* db, cudaStream_t st);
+
+struct FwdArgs {
+  const uint16_t* x;
+  int T;
+  const int32_t* table;
+  uint16_t* y;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* perm_out;     // may be null
+  int32_t* offsets_out;  // may be null
+};
+
+// One-time kernel attributes (dynamic shared memory limits); called by
+// moe_reserve so that moe_forward makes no such call (graph capture).
+cudaError_t prepare_router(const Ctx& c);
+cudaError_t prepare_general_experts(const Ctx& c);
+
+cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
+                                   int* launches);
+
+}  // namespace moe

@@ -1,0 +1,176 @@
+// permute.cu -- deterministic token->expert permutation (stable counting sort).
+//
+// The pairs p = t*k + j (token t's j-th expert) are sorted by expert id,
+// keeping ascending p inside each expert: offsets[e] = number of pairs with a
+// smaller expert id, perm[offsets[e] + r] = the r-th pair (in p order) that
+// chose e, inv[p] = the position of p in perm.  `used` lists the experts with
+// at least one pair in ascending id; the expert kernels walk it.
+#include "device_util.cuh"
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kPairsPerBlock = 2048;
+
+// Exclusive scan of one value per thread over a CTA of up to 1024 threads.
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < nw) warp_tot[lane] = w;  // inclusive warp prefix
+    if (lane == nw - 1) *total = w;
+  }
+  __syncthreads();
+  const int before = warp ? warp_tot[warp - 1] : 0;
+  const int r = before + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// Stable placement of pairs [p0, p1) by one warp, in order, chunk by chunk:
+// pos[e] holds the next free position of expert e.
+__device__ void warp_stable_scatter(const int32_t* __restrict__ topk_idx, int p0, int p1,
+                                    int* pos, int32_t* __restrict__ perm,
+                                    int32_t* __restrict__ inv, int32_t* perm_out) {
+  const int lane = threadIdx.x & 31;
+  for (int base = p0; base < p1; base += 32) {
+    const int p = base + lane;
+    const int e = p < p1 ? topk_idx[p] : -1;
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(mask & ((1u << lane) - 1u));
+    int q = 0;
+    if (e >= 0) q = pos[e] + rank;
+    __syncwarp();
+    if (e >= 0) {
+      perm[q] = p;
+      inv[p] = q;
+      if (perm_out) perm_out[q] = p;
+      if (lane == 31 - __clz(mask)) pos[e] += __popc(mask);
+    }
+    __syncwarp();
+  }
+}
+
+// One CTA does everything (used when the pairs fit one block).
+__global__ void __launch_bounds__(1024) permute_small_kernel(
+    const int32_t* __restrict__ topk_idx, int P, int E, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ used,
+    int32_t* __restrict__ n_used, int32_t* perm_out, int32_t* offsets_out) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int warp_tot[32];
+  __shared__ int total, total_used;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) atomicAdd(&cnt[topk_idx[p]], 1);
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = e < E ? cnt[e] : 0;
+  const int excl = block_exclusive_scan(c, warp_tot, &total);
+  const int uexcl = block_exclusive_scan(c > 0 ? 1 : 0, warp_tot, &total_used);
+  if (e < E) {
+    offsets[e] = excl;
+    if (offsets_out) offsets_out[e] = excl;
+    if (c > 0) used[uexcl] = e;
+    cnt[e] = excl;
+  }
+  if (e == 0) {
+    offsets[E] = total;
+    if (offsets_out) offsets_out[E] = total;
+    *n_used = total_used;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) warp_stable_scatter(topk_idx, 0, P, cnt, perm, inv, perm_out);
+}
+
+// Large P, pass 1: per-block expert counts.
+__global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ topk_idx,
+                                                            int P, int E,
+                                                            int32_t* __restrict__ hist) {
+  __shared__ int cnt[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kPairsPerBlock, p1 = min(P, p0 + kPairsPerBlock);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&cnt[topk_idx[p]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// Large P, pass 2: offsets, used list, and each block's first position per expert.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(
+    int32_t* __restrict__ hist, int nblk, int E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ used, int32_t* __restrict__ n_used, int32_t* offsets_out) {
+  __shared__ int warp_tot[32];
+  __shared__ int total, total_used;
+  const int e = threadIdx.x;
+  int running = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int v = hist[(size_t)b * E + e];
+      hist[(size_t)b * E + e] = running;
+      running += v;
+    }
+  }
+  const int excl = block_exclusive_scan(running, warp_tot, &total);
+  const int uexcl = block_exclusive_scan(running > 0 ? 1 : 0, warp_tot, &total_used);
+  if (e < E) {
+    offsets[e] = excl;
+    if (offsets_out) offsets_out[e] = excl;
+    if (running > 0) used[uexcl] = e;
+    for (int b = 0; b < nblk; ++b) hist[(size_t)b * E + e] += excl;
+  }
+  if (e == 0) {
+    offsets[E] = total;
+    if (offsets_out) offsets_out[E] = total;
+    *n_used = total_used;
+  }
+}
+
+// Large P, pass 3: stable scatter of each block's pairs by one warp.
+__global__ void __launch_bounds__(32) permute_scatter_kernel(
+    const int32_t* __restrict__ topk_idx, int P, int E, const int32_t* __restrict__ hist,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* perm_out) {
+  __shared__ int pos[kMaxE];
+  for (int e = threadIdx.x; e < E; e += 32) pos[e] = hist[(size_t)blockIdx.x * E + e];
+  __syncwarp();
+  const int p0 = blockIdx.x * kPairsPerBlock, p1 = min(P, p0 + kPairsPerBlock);
+  warp_stable_scatter(topk_idx, p0, p1, pos, perm, inv, perm_out);
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches) {
+  const int P = a.T * c.d.k, E = c.d.E;
+  if (P <= kPairsPerBlock) {
+    permute_small_kernel<<<1, 1024, 0, st>>>(a.topk_idx, P, E, c.ws.perm, c.ws.inv,
+                                              c.ws.offsets, c.ws.used, c.ws.n_used, a.perm_out,
+                                              a.offsets_out);
+    ++*launches;
+    return cudaGetLastError();
+  }
+  const int nblk = (P + kPairsPerBlock - 1) / kPairsPerBlock;
+  permute_count_kernel<<<nblk, 256, 0, st>>>(a.topk_idx, P, E, c.ws.hist);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(c.ws.hist, nblk, E, c.ws.offsets, c.ws.used,
+                                           c.ws.n_used, a.offsets_out);
+  permute_scatter_kernel<<<nblk, 32, 0, st>>>(a.topk_idx, P, E, c.ws.hist, c.ws.perm, c.ws.inv,
+                                               a.perm_out);
+  *launches += 3;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

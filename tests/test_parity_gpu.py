@@ -1,0 +1,246 @@
+"""GPU parity of the CUDA library against the CPU oracle (all through the C ABI)."""
+import numpy as np
+import pytest
+
+import int4_routed_expert_decode_gb300 as moe
+import synth
+from oracle import moe_oracle as O
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+W0 = synth.WORKLOADS[0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int4_routed_expert_decode_gb300 import build
+    build.build()
+    import torch
+    assert torch.cuda.is_available()
+    torch.cuda.init()
+
+
+def _weights(wl, layer=0):
+    return synth.layer_weights(0, wl.wid, layer, wl.shape, zipf_s=wl.zipf_s)
+
+
+def _x(wl, T, layer=0, step=0):
+    return synth.tokens(0, wl.wid, layer, step, T, wl.H)
+
+
+# ------------------------------------------------------------------ tiny workload
+@pytest.mark.parametrize("path", [moe.MOE_PATH_AUTO, moe.MOE_PATH_GENERAL])
+def test_tiny_workload_parity(path):
+    W = _weights(W0)
+    x = _x(W0, W0.T)
+    L = U.layer(W0.shape, W, max_T=W0.T)
+    moe.moe_set_path(L.ctx, path)
+    out = U.run(L, x)
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    U.assert_parity(out, ref, what="tiny")
+
+
+@pytest.mark.parametrize("T", [1, 3, 31, 64, 65, 200])
+def test_tiny_shapes_ragged_token_counts(T):
+    """Token counts across the decode / general boundary and several tiles."""
+    W = _weights(W0, layer=1)
+    x = _x(W0, T, layer=1, step=T)
+    L = U.layer(W0.shape, W, max_T=256)
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    U.assert_parity(U.run(L, x), ref, what=f"T={T}")
+
+
+def test_tiny_with_zipf_prior_and_larger_k():
+    shape = synth.Shape(E=16, k=5, H=256, I=64, Is=128, G=32)
+    W = synth.layer_weights(0, 0, 7, shape, zipf_s=1.1)
+    x = synth.tokens(0, 0, 7, 0, 40, shape.H)
+    L = U.layer(shape, W, max_T=40)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="zipf k=5 Is=128")
+
+
+def test_group_128_and_wide_hidden():
+    shape = synth.Shape(E=32, k=4, H=1024, I=256, Is=128, G=128)
+    W = synth.layer_weights(0, 0, 9, shape)
+    x = synth.tokens(0, 0, 9, 0, 9, shape.H)
+    L = U.layer(shape, W, max_T=9)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="G=128")
+
+
+def test_k_equals_E_dense_mixture():
+    shape = synth.Shape(E=8, k=8, H=256, I=64, Is=64, G=32)
+    W = synth.layer_weights(0, 0, 3, shape)
+    x = synth.tokens(0, 0, 3, 0, 5, shape.H)
+    L = U.layer(shape, W, max_T=5)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="k=E")
+
+
+# ------------------------------------------------------------------ exact routing
+def test_exact_ties_go_to_lowest_index():
+    """Identical router rows: every logit ties; the GPU must take experts 0..k-1."""
+    W = _weights(W0)
+    W["router_w"] = np.repeat(W["router_w"][:1], W0.E, axis=0)
+    x = _x(W0, 6)
+    L = U.layer(W0.shape, W, max_T=6)
+    out = U.run(L, x)
+    assert out["topk_idx"].tolist() == [list(range(W0.k))] * 6
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    U.assert_parity(out, ref, what="ties")
+
+
+def test_near_ties_one_ulp_apart():
+    """Rows equal but for one bf16 ulp: fp32 logits tie or nearly; exact order decides."""
+    W = _weights(W0)
+    rw = W["router_w"].copy()
+    for e in range(1, W0.E):
+        rw[e] = rw[0]
+        rw[e, e % W0.H] ^= 1  # one ulp at a different column per expert
+    W["router_w"] = rw
+    x = _x(W0, 16, step=5)
+    L = U.layer(W0.shape, W, max_T=16)
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    U.assert_parity(U.run(L, x), ref, what="near ties")
+
+
+def test_duplicate_rows_with_prior():
+    shape = synth.Shape(E=64, k=6, H=256, I=64, Is=64, G=32)
+    W = synth.layer_weights(0, 0, 11, shape, zipf_s=0.0)
+    rw = W["router_w"]
+    rw[10:20] = rw[3]
+    W["router_bias"] = np.zeros(shape.E, np.float32)
+    x = synth.tokens(0, 0, 11, 0, 12, shape.H)
+    L = U.layer(shape, W, max_T=12)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="duplicate rows")
+
+
+# ------------------------------------------------------------------ placement, repack, errors
+def test_placement_invariance_bit_identical():
+    """Experts loaded in a permuted slot order with the matching table answer identically."""
+    W = _weights(W0)
+    x = _x(W0, 8)
+    L1 = U.layer(W0.shape, W, max_T=8)
+    a = U.run(L1, x)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(W0.E)          # slot s holds expert order[s]
+    Wp = dict(W)
+    Wp["experts"] = {k: np.ascontiguousarray(v[order]) for k, v in W["experts"].items()}
+    table = np.empty(W0.E, np.int32)
+    table[order] = np.arange(W0.E, dtype=np.int32)
+    L2 = U.layer(W0.shape, Wp, max_T=8)
+    b = U.run(L2, x, table=table)
+    for key in ("y_bits", "topk_idx", "topk_w", "perm", "offsets"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_partial_pool_with_slot_table():
+    """A pool holding only the selected experts (n_slots < E) gives the same answer."""
+    W = _weights(W0)
+    x = _x(W0, 4)
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    need = sorted(set(ref["topk_idx"].ravel().tolist()))
+    Wp = dict(W)
+    Wp["experts"] = {k: np.ascontiguousarray(v[need]) for k, v in W["experts"].items()}
+    table = np.full(W0.E, -1, np.int32)
+    table[need] = np.arange(len(need), dtype=np.int32)
+    L = U.layer(W0.shape, Wp, max_T=4, n_slots=len(need))
+    U.assert_parity(U.run(L, x, table=table), ref, what="partial pool")
+
+
+def test_repack_round_trip_bytes():
+    W = _weights(W0)
+    L = U.layer(W0.shape, W, max_T=1)
+    for slot in (0, 7, W0.E - 1):
+        back = moe.moe_read_expert(L.ctx, slot, W0.H, W0.I, W0.G)
+        for key, v in back.items():
+            assert np.array_equal(v, W["experts"][key][slot]), (slot, key)
+    back = moe.moe_read_expert(L.ctx, -1, W0.H, W0.Is, W0.G)
+    for key, v in back.items():
+        assert np.array_equal(v, W["shared"][key][0]), ("shared", key)
+
+
+def test_device_pointer_weights_match_host_pointer_weights():
+    W = _weights(W0)
+    x = _x(W0, 4)
+    a = U.run(U.layer(W0.shape, W, max_T=4), x)
+    b = U.run(U.layer(W0.shape, W, max_T=4, device_weights=True), x)
+    assert np.array_equal(a["y_bits"], b["y_bits"])
+
+
+def test_missing_slot_is_reported_not_faulted():
+    W = _weights(W0)
+    x = _x(W0, 4)
+    L = U.layer(W0.shape, W, max_T=4)
+    table = np.arange(W0.E, dtype=np.int32)
+    table[:] = -1
+    out = U.run(L, x, table=table)
+    assert out["status"] == moe.MOE_ERR_SLOT
+    # the sticky word is cleared by the read: a good call reports OK again
+    out = U.run(L, x)
+    assert out["status"] == moe.MOE_OK
+
+
+def test_host_side_argument_errors():
+    import torch
+    W = _weights(W0)
+    L = U.layer(W0.shape, W, max_T=4)
+    x = torch.zeros((8, W0.H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as e:
+        L.forward(x)
+    assert e.value.status == moe.MOE_ERR_NOT_RESERVED
+    y = torch.zeros((4, W0.H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_forward(L.ctx, y, 4, None, y, torch.zeros(8, dtype=torch.int32, device="cuda"),
+                        torch.zeros(8, device="cuda"))
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    # T = 0 is a no-op
+    moe.moe_forward(L.ctx, x, 0, None, y, None, None)
+
+
+def test_batch_equals_single_token_calls():
+    """Incremental (one token per call) vs whole batch: same experts, y within tolerance."""
+    W = _weights(W0, layer=2)
+    x = _x(W0, 12, layer=2)
+    L = U.layer(W0.shape, W, max_T=12)
+    full = U.run(L, x)
+    for t in range(12):
+        one = U.run(L, x[t:t + 1])
+        assert np.array_equal(one["topk_idx"][0], full["topk_idx"][t])
+        U.assert_y_close(one["y"][0], full["y"][t], what=f"token {t}")
+
+
+# ------------------------------------------------------------------ full-size single layers
+@pytest.mark.parametrize("wid", [1, 2])
+def test_decode_workload_single_layer(wid):
+    wl = synth.WORKLOADS[wid]
+    W = _weights(wl, layer=0)
+    L = U.layer(wl.shape, W, max_T=4)
+    for step in range(3):
+        x = _x(wl, 1, layer=0, step=step)
+        ref = O.moe_block(x, W, wl.k, wl.G)
+        U.assert_parity(U.run(L, x), ref, what=f"wl{wid} step{step}")
+
+
+def test_batched_decode_zipf_workload():
+    wl = synth.WORKLOADS[3]
+    W = _weights(wl)
+    x = _x(wl, wl.T)
+    L = U.layer(wl.shape, W, max_T=wl.T)
+    ref = O.moe_block(x, W, wl.k, wl.G)
+    U.assert_parity(U.run(L, x), ref, what="batch64")
+
+
+def test_prefill_zipf_workload_sampled_rows():
+    """T = 4096: every index and the permutation bit-exact, y on 48 sampled tokens."""
+    wl = synth.WORKLOADS[4]
+    W = _weights(wl)
+    x = _x(wl, wl.T)
+    L = U.layer(wl.shape, W, max_T=wl.T)
+    out = U.run(L, x)
+    rows = np.random.default_rng(4).choice(wl.T, 48, replace=False)
+    rows = sorted(rows.tolist() + [0, wl.T - 1])
+    ref = O.moe_block(x, W, wl.k, wl.G, tokens=rows)
+    U.assert_parity(out, ref, rows=rows, what="prefill")
