@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the int4 routed-expert MoE block on GB300.
+
+Metric: MoE-layer tokens/s (token passes through one MoE layer per second)
+and the achieved HBM bandwidth, unique expert bytes touched / time, against
+the measured copy bandwidth.  The default workload is the 35B-class decode
+stack: E=256, k=8, hidden 2048, inter 512, group 64, 40 layers, one token per
+step, each layer with its own weights (18.2 GB resident).
+
+One step = one token through all the stacked layers, replayed from a CUDA
+graph of the library's launch sequence; the inputs of 16 distinct steps
+rotate, and every step touches far more distinct expert bytes than the L2
+holds.  Rank 0 prints one JSON line.
+
+  python bench.py [--steps K] [--warmup W] [--workload 1]     # our CUDA path
+  python bench.py --impl reference                            # the CPU oracle
+Under torchrun each rank runs an independent replica (no collective on the
+data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s vs peak (int4 experts, 1 GB300)"
+UNIT = "layer-tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", type=int, default=1)
+    p.add_argument("--layers", type=int, default=None, help="override the stack depth")
+    p.add_argument("--distinct", type=int, default=16, help="distinct step inputs")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", type=int, default=0, help="kernel path (0 auto)")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [s.strip() for s in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# --------------------------------------------------------------------- oracle timing
+def oracle_units(wl, budget_s, layers, check=None):
+    """Time the CPU oracle on (layer, token) passes of the workload for about
+    budget_s seconds.  Returns (passes/s, passes, seconds, sample text, results)."""
+    from oracle import moe_oracle as O
+    n_layers = min(layers, 2)
+    Ws = [synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s) for l in range(n_layers)]
+    tok = 1 if wl.T == 1 else min(wl.T, 8)
+    done, results = 0, []
+    t0 = time.perf_counter()
+    step = 0
+    while True:
+        l = step % n_layers
+        x = synth.tokens(0, wl.wid, l, step // n_layers, wl.T, wl.H)
+        rows = list(range(tok))
+        r = O.moe_block(x, Ws[l], wl.k, wl.G, tokens=rows)
+        results.append((l, step // n_layers, rows, r))
+        done += tok
+        step += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"{done} (layer, token) passes of the CPU oracle over layers 0..{n_layers - 1}, "
+              f"{tok} token(s) per pass" + ("" if wl.T == 1 else f" of a {wl.T}-token batch"))
+    return done / dt, done, dt, sample, results
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import moe_oracle as O
+    L = args.layers or wl.layers
+    n_layers = min(L, 2)
+    Ws = [synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s) for l in range(n_layers)]
+    tok = 1 if wl.T == 1 else min(wl.T, 8)
+
+    def step(i):
+        l = i % n_layers
+        x = synth.tokens(0, wl.wid, l, i // n_layers, wl.T, wl.H)
+        O.moe_block(x, Ws[l], wl.k, wl.G, tokens=list(range(tok)))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps * tok / dt
+    sample = f"each step: {tok} token(s) through one MoE layer (layers 0..{n_layers - 1} alternate)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": config_of(wl, L, note="CPU oracle (numpy float64), bounded sample per step"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, L, note=None):
+    c = {"workload": wl.name, "E": wl.E, "k": wl.k, "hidden": wl.H, "inter": wl.I,
+         "shared_inter": wl.Is, "group": wl.G, "tokens_per_step": wl.T, "layers": L,
+         "zipf_s": wl.zipf_s, "weights": "int4 affine (bf16 scale+bias per group), seeded synthetic",
+         "parallelism": "replicas"}
+    if note:
+        c["note"] = note
+    return c
+
+
+# --------------------------------------------------------------------- our arm
+def run_ours(args, wl):
+    import torch
+
+    import int4_routed_expert_decode_gb300 as moe
+    from int4_routed_expert_decode_gb300 import build as moe_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    moe_build.build()
+    L = args.layers or wl.layers
+    T, H = wl.T, wl.H
+    S = max(1, min(args.distinct, args.steps + args.warmup))
+    layers = []
+    for l in range(L):
+        W = synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s)
+        layer = moe.MoELayer(wl.E, wl.k, H, wl.I, wl.Is, wl.G, weights=W, max_T=T)
+        if args.path:
+            moe.moe_set_path(layer.ctx, args.path)
+        layers.append(layer)
+        del W
+    x_all = torch.empty((S, L, T, H), dtype=torch.bfloat16, device="cuda")
+    for s in range(S):
+        for l in range(L):
+            xs = synth.tokens(0, wl.wid, l, s, T, H)
+            x_all[s, l].copy_(torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16))
+    y = torch.empty((L, T, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((L, T, wl.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((L, T, wl.k), dtype=torch.float32, device="cuda")
+    x_in = torch.empty((L, T, H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def enqueue(xsrc):
+        for l in range(L):
+            moe.moe_forward(layers[l].ctx, xsrc[l], T, None, y[l], idx[l], wts[l],
+                            stream=stream.cuda_stream)
+
+    # eager pass per distinct input: statuses, unique experts, launch count
+    uniq_bytes = []
+    ys0 = None
+    with torch.cuda.stream(stream):
+        for s in range(S):
+            enqueue(x_all[s])
+            stream.synchronize()
+            if s == 0:
+                ys0 = y.clone()
+            ids = idx.cpu().numpy()
+            uniq_bytes.append(sum(len(set(ids[l].ravel().tolist())) * wl.expert_bytes +
+                                  wl.shared_bytes for l in range(L)))
+    for l in range(L):
+        st = layers[l].status(stream.cuda_stream)
+        if st != moe.MOE_OK:
+            raise RuntimeError(f"layer {l}: {moe.moe_status_string(st)}")
+    launches_per_layer = moe.moe_last_launch_count(layers[-1].ctx)
+    unique_per_step = float(np.mean(uniq_bytes))
+
+    graphs = []
+    for s in range(S):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            enqueue(x_all[s])
+        graphs.append(g)
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        enqueue(x_in)
+
+    clocks = ClockSampler(local).start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % S].replay()
+        stream.synchronize()
+        # keep the GPU loaded ~1 s so that clock samples exist before timing
+        t_load = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_load < 1.0:
+            graphs[i % S].replay()
+            i += 1
+            if i % 64 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[(args.warmup + i) % S].replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    t_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    sec = t_max / 1e3
+    value = world * T * L * args.steps / sec
+    ms_step = t_max / args.steps
+    us_layer = ms_step * 1e3 / L
+    hbm = unique_per_step / (ms_step / 1e3) / 1e9
+    pk = peaks()
+
+    # e2e through the C ABI with host buffers: H2D x, graph, D2H y every step
+    x_host = torch.empty((L, T, H), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x_all[0].cpu())
+    y_host = torch.empty((L, T, H), dtype=torch.bfloat16, pin_memory=True)
+    k_e2e = max(1, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x_in.copy_(x_host, non_blocking=True)
+            g_e2e.replay()
+            y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            x_in.copy_(x_host, non_blocking=True)
+            g_e2e.replay()
+            y_host.copy_(y, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / k_e2e
+    e2e_value = world * T * L / (ms_e2e / 1e3)
+
+    # CPU oracle on the host cores (rank 0, N = 1), and a parity spot check
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, dt, sample, results = oracle_units(wl, args.cpu_budget, L)
+        cpu = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+               "sample": sample + f", {dt:.1f} s"}
+        # results of (layer l, input step s) for s < S can be checked against the eager pass
+        errs = []
+        for (l, s, rows, r) in results:
+            if s == 0:
+                yg = ys0[l, rows].float().cpu().numpy().astype(np.float64)
+                d = np.abs(yg - r["y"])
+                errs.append(float(d.max() / np.abs(r["y"]).max()))
+        if errs:
+            parity = {"checked_passes": len(errs), "max_rel_err": max(errs)}
+
+    algo_bytes_layer = unique_per_step / L + wl.router_bytes + 2 * T * H * 2
+    achieved = algo_bytes_layer / (us_layer * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "kernel": f"one layer of moe_forward ({launches_per_layer} launches), "
+                          f"{algo_bytes_layer / 1e6:.2f} MB algorithmic per layer",
+                "peak_source": pk["source"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": config_of(wl, L, note="inputs larger than L2: each step touches "
+                            f"{unique_per_step / 1e6:.0f} MB of distinct expert weights; "
+                            f"{S} distinct step inputs rotate"),
+        "us_per_layer": us_layer, "stack_tokens_per_s": world * T / (ms_step / 1e3),
+        "hbm_gbs_unique_expert_bytes": hbm, "hbm_frac": hbm / pk["hbm_gbs"],
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": L * T * H * 2,
+                "d2h_bytes_per_step": L * T * H * 2},
+        "clocks": clk, "gpu_launches": args.steps * L * launches_per_layer,
+        "parity_spot_check": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for layer in layers:
+        layer.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()
