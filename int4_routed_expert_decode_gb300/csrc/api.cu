@@ -146,6 +146,14 @@ int load_experts(moe_ctx* ctx, const moe_qmatrix& g, const moe_qmatrix& u, const
 
 }  // namespace
 
+namespace moe {
+// Message of a context-free entry point, read back by moe_last_error(NULL).
+int set_global_msg(int code, const char* text) {
+  snprintf(g_create_msg, sizeof(g_create_msg), "%s", text);
+  return code;
+}
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_status_string(int status) {

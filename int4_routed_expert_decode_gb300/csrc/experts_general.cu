@@ -21,6 +21,7 @@ namespace {
 constexpr int kTC = 8;         // tokens staged per pass
 constexpr int kRowsPerCta = 32;
 constexpr int kWarps = 8;
+constexpr int kStageBudget = 96 * 1024;  // bytes of staged vectors per CTA
 
 struct Unit {
   const uint8_t* blob;  // null: nothing to do
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 }
 
 int pick_tc(int K) {
-  const int budget = 96 * 1024;
+  const int budget = kStageBudget;
   int tc = budget / (K * 4 + (K / 32) * 4);
   return max(1, min(kTC, tc));
 }
@@ -216,16 +217,16 @@ int pick_tc(int K) {
 }  // namespace
 
 cudaError_t prepare_general_experts(const Ctx& c) {
-  const Dims& d = c.d;
-  const int maxI = d.I > d.Is ? d.I : d.Is;
-  int tc = pick_tc(d.H);
+  // The limits are per kernel, not per context: size them for the largest
+  // staging any shape can ask for (pick_tc keeps it within its budget), so
+  // that preparing one context never lowers the limit under another.
+  (void)c;
+  const int most = kStageBudget + 1024;
   cudaError_t e = cudaFuncSetAttribute(gateup_general_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)((size_t)tc * d.H * 4 + (size_t)tc * (d.H / 32) * 4));
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, most);
   if (e != cudaSuccess) return e;
-  tc = pick_tc(maxI);
   return cudaFuncSetAttribute(down_general_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)((size_t)tc * maxI * 4 + (size_t)tc * (maxI / 32) * 4));
+                              most);
 }
 
 cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,

@@ -103,4 +103,7 @@ cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int*
 cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
 
+// Set the message returned by moe_last_error(NULL); returns `code`.
+int set_global_msg(int code, const char* text);
+
 }  // namespace moe

@@ -389,7 +389,9 @@ cudaError_t prepare_router(const Ctx& c) {
       return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  const size_t tsmem = ((size_t)c.d.E * 8 + (kRunCache + 2) * kDigits * 4) * kTopkWarps;
+  // The limit is per kernel, not per context: size it for the largest E so
+  // that preparing a small context never lowers it under a larger one.
+  const size_t tsmem = ((size_t)kMaxE * 8 + (kRunCache + 2) * kDigits * 4) * kTopkWarps;
   return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tsmem);
 }
@@ -407,3 +409,4 @@ cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* la
 }
 
 }  // namespace moe
+
