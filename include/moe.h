@@ -160,6 +160,39 @@ int64_t moe_device_bytes(const moe_ctx* ctx);
 /* Number of kernel launches the last moe_forward enqueued. */
 int moe_last_launch_count(const moe_ctx* ctx);
 
+/* Allocation-free routing: router logits, exact top-k with renormalised
+ * weights, and the shared-expert sigmoid gate for T tokens, with no context
+ * and no device allocation of any kind.  The pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc -- code whose
+ * device memory belongs to a host application's own allocator, code that
+ * must not trigger the device synchronisation an allocation can cause, or
+ * code that may only enqueue work on streams it is given.
+ *   x              bf16 [T][hidden] device, 16-byte aligned
+ *   router_w       bf16 [E][hidden] device, 16-byte aligned
+ *   router_bias    fp32 [E] device, or NULL (no prior)
+ *   shared_gate_w  bf16 [hidden] device, 16-byte aligned
+ *   topk_idx       int32 [T][k] device, written (same contract as moe_forward)
+ *   topk_w         fp32 [T][k] device, written
+ *   shared_gate    fp32 [T] device, written: sigmoid(x_t . shared_gate_w)
+ * Sizes: E in [1, 1024], k in [1, min(E, 32)], hidden a multiple of 256 up to
+ * 8192, T in [0, MOE_STATIC_ROUTE_MAX_T] and T*E <= MOE_STATIC_ROUTE_MAX_LOGITS;
+ * larger sizes return MOE_ERR_INVALID_ARG with a message for
+ * moe_last_error(NULL).
+ * Scratch: the intermediates live in one file-scope device array of
+ * (2 * MOE_STATIC_ROUTE_MAX_LOGITS + MOE_STATIC_ROUTE_MAX_T) floats (1 MiB +
+ * 16 KiB), held by every device that loads the library until the process
+ * exits.  The first call on a device looks up that array's device address
+ * and sets kernel attributes; make it before any stream capture.  Every call
+ * shares the one array: calls whose kernels overlap on the GPU (different
+ * streams without ordering between them) race and give undefined results;
+ * calls in one stream, or otherwise ordered, are safe.  Asynchronous on
+ * `stream`. */
+#define MOE_STATIC_ROUTE_MAX_LOGITS 131072
+#define MOE_STATIC_ROUTE_MAX_T 4096
+int moe_route_static(const void* x, int T, const uint16_t* router_w, const float* router_bias,
+                     const uint16_t* shared_gate_w, int E, int k, int hidden, int32_t* topk_idx,
+                     float* topk_w, float* shared_gate, void* stream);
+
 const char* moe_last_error(const moe_ctx* ctx);
 const char* moe_status_string(int status);
 

@@ -33,6 +33,7 @@ EXPORTS = (
     "moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
     "moe_read_expert", "moe_set_path", "moe_expert_blob_bytes", "moe_device_bytes",
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
+    "moe_route_static",
 )
 
 
@@ -88,6 +89,8 @@ def lib():
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_destroy.argtypes = [vp]
     L.moe_destroy.restype = None
+    L.moe_route_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
+    L.moe_route_static.restype = i32
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
                  "moe_read_expert", "moe_set_path", "moe_last_launch_count"):
         getattr(L, name).restype = i32
@@ -229,6 +232,14 @@ def moe_status_string(status: int) -> str:
 
 def moe_destroy(ctx: int):
     lib().moe_destroy(ctx)
+
+
+def moe_route_static(x, T: int, router_w, router_bias, shared_gate_w, E: int, k: int,
+                     hidden: int, topk_idx, topk_w, shared_gate, stream=None):
+    """Routing with no allocation (library-owned static scratch); see include/moe.h."""
+    _check(lib().moe_route_static(_addr(x), T, _addr(router_w), _addr(router_bias),
+                                  _addr(shared_gate_w), E, k, hidden, _addr(topk_idx),
+                                  _addr(topk_w), _addr(shared_gate), _stream(stream)))
 
 
 # ----------------------------------------------------------------- convenience

@@ -10,6 +10,9 @@
 // going to the lower expert id.  The weights are the softmax probabilities
 // of the k selected experts renormalised to sum to one, i.e.
 // w_j = exp(l_j - m) / sum_i exp(l_i - m) over the selected i.
+#include <cstdio>
+#include <mutex>
+
 #include "device_util.cuh"
 #include "moe_internal.cuh"
 
@@ -410,3 +413,129 @@ cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* la
 
 }  // namespace moe
 
+// ---------------------------------------------------------------------------
+// Allocation-free routing (moe_route_static).
+//
+// Some callers cannot call cudaMalloc at all: code whose device memory is
+// owned by a host application's own allocator, code that must not trigger
+// the implicit synchronisation an allocation can cause, code that only
+// enqueues work onto streams it is handed.  For them this entry point runs
+// the same router and top-k kernels as moe_forward, taking every input and
+// output from the caller and keeping its intermediates (fp32 logits, their
+// error bounds, the shared-gate pre-activations) in the file-scope device
+// array below.  The array is loaded with the library and stays resident on
+// every device that loads it until the process exits.
+namespace moe {
+namespace {
+
+constexpr int kStaticMaxLogits = MOE_STATIC_ROUTE_MAX_LOGITS;  // T * E
+constexpr int kStaticMaxT = MOE_STATIC_ROUTE_MAX_T;
+constexpr int kStaticMaxDevices = 64;
+
+// [0, kStaticMaxLogits): logits, [kStaticMaxLogits, 2*kStaticMaxLogits):
+// bounds, then kStaticMaxT shared-gate pre-activations.  Every call writes
+// each element it later reads, so nothing needs clearing between calls.
+static __device__ __align__(256) float g_route_scratch[2 * kStaticMaxLogits + kStaticMaxT];
+
+std::mutex g_static_mu;
+float* g_static_ptr[kStaticMaxDevices] = {};
+
+// Once per device, with that device current: the device address of the
+// array (its host-side name is only a stand-in) and the kernels' dynamic
+// shared-memory limits.
+cudaError_t static_route_setup(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    float* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_route_scratch);
+    if (e != cudaSuccess) return e;
+    const int max_smem_router = kRouterTC * kMaxH * 2;
+    const cudaError_t attrs[] = {
+        cudaFuncSetAttribute(router_logits_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(router_logits_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(router_logits_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(router_logits_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(router_logits_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(router_logits_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_router),
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(((size_t)kMaxE * 8 + (kRunCache + 2) * kDigits * 4) * kTopkWarps))};
+    for (cudaError_t a : attrs)
+      if (a != cudaSuccess) return a;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route_static(const void* x, int T, const uint16_t* router_w,
+                                const float* router_bias, const uint16_t* shared_gate_w, int E,
+                                int k, int hidden, int32_t* topk_idx, float* topk_w,
+                                float* shared_gate, void* stream) {
+  using namespace moe;
+  char msg[256];
+  if (T < 0 || T > kStaticMaxT) {
+    snprintf(msg, sizeof msg, "moe_route_static: T=%d not in [0, %d]", T, kStaticMaxT);
+    return set_global_msg(MOE_ERR_INVALID_ARG, msg);
+  }
+  if (E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) {
+    snprintf(msg, sizeof msg, "moe_route_static: E=%d, k=%d out of range", E, k);
+    return set_global_msg(MOE_ERR_INVALID_ARG, msg);
+  }
+  if (hidden < 256 || hidden > kMaxH || hidden % 256 != 0) {
+    snprintf(msg, sizeof msg, "moe_route_static: hidden=%d must be a multiple of 256 in [256, %d]",
+             hidden, kMaxH);
+    return set_global_msg(MOE_ERR_UNSUPPORTED, msg);
+  }
+  if ((int64_t)T * E > kStaticMaxLogits) {
+    snprintf(msg, sizeof msg,
+             "moe_route_static: T*E=%lld exceeds the static scratch limit of %d logits",
+             (long long)T * E, kStaticMaxLogits);
+    return set_global_msg(MOE_ERR_INVALID_ARG, msg);
+  }
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !shared_gate_w || !topk_idx || !topk_w || !shared_gate)
+    return set_global_msg(MOE_ERR_INVALID_ARG, "moe_route_static: a required pointer is NULL");
+  if ((((uintptr_t)x) | ((uintptr_t)router_w) | ((uintptr_t)shared_gate_w)) & 15)
+    return set_global_msg(MOE_ERR_INVALID_ARG,
+                          "moe_route_static: x, router_w and shared_gate_w must be 16-byte aligned");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices)
+    return set_global_msg(MOE_ERR_CUDA, "moe_route_static: no usable current device");
+  float* base = nullptr;
+  e = static_route_setup(dev, &base);
+  if (e != cudaSuccess) {
+    snprintf(msg, sizeof msg, "moe_route_static: set-up failed: %s", cudaGetErrorString(e));
+    return set_global_msg(MOE_ERR_CUDA, msg);
+  }
+  float* logits = base;
+  float* bound = base + kStaticMaxLogits;
+  float* gate_z = base + 2 * kStaticMaxLogits;
+  cudaStream_t st = (cudaStream_t)stream;
+  const uint16_t* xb = (const uint16_t*)x;
+  const int grid = (E + 1 + kRouterWarps - 1) / kRouterWarps;
+  const size_t smem = (size_t)kRouterTC * hidden * 2;
+  switch (hidden / 256) {
+    case 1: router_logits_kernel<1><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    case 2: router_logits_kernel<2><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    case 4: router_logits_kernel<4><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    case 8: router_logits_kernel<8><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    case 16: router_logits_kernel<16><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    case 32: router_logits_kernel<32><<<grid, kRouterWarps * 32, smem, st>>>(xb, T, router_w, router_bias, shared_gate_w, E, logits, bound, gate_z); break;
+    default:
+      return set_global_msg(MOE_ERR_UNSUPPORTED, "moe_route_static: unsupported hidden size");
+  }
+  const size_t tsmem = ((size_t)E * 8 + (kRunCache + 2) * kDigits * 4) * kTopkWarps;
+  topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, tsmem, st>>>(
+      logits, bound, gate_z, xb, router_w, router_bias, T, E, hidden, k, topk_idx, topk_w,
+      shared_gate);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    snprintf(msg, sizeof msg, "moe_route_static: launch failed: %s", cudaGetErrorString(e));
+    return set_global_msg(MOE_ERR_CUDA, msg);
+  }
+  return MOE_OK;
+}
