@@ -147,10 +147,21 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
                     uint32_t* up_q, uint16_t* up_s, uint16_t* up_b, uint32_t* down_q,
                     uint16_t* down_s, uint16_t* down_b);
 
-/* Kernel path of moe_forward: MOE_PATH_AUTO picks by T (decode kernels up
- * to 64 tokens, grouped GEMM above); the others force one path. */
+/* Kernel path of moe_forward.  MOE_PATH_AUTO uses the fused single-launch
+ * decode kernel for T = 1 when the sizes allow it (hidden in {256, 512,
+ * 1024, 2048}, inter == shared_inter <= 1024) and the general kernels
+ * otherwise; MOE_PATH_DECODE insists on the fused kernel (MOE_ERR_UNSUPPORTED
+ * if it cannot run); MOE_PATH_GENERAL forces the general kernels. */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_GENERAL = 2, MOE_PATH_PREFILL = 3 };
 int moe_set_path(moe_ctx* ctx, int path);
+
+/* Test hooks, off by default.  MOE_TEST_BARRIER_TIMEOUT makes the grid
+ * barriers of the fused decode kernel wait for one arrival more than the
+ * grid has: the bounded wait runs out (about one second), the device records
+ * MOE_ERR_TIMEOUT, and moe_get_status reports it and resets the barrier so
+ * that the context stays usable.  flags = 0 turns every hook off. */
+enum { MOE_TEST_BARRIER_TIMEOUT = 1 };
+int moe_set_test_flags(moe_ctx* ctx, int flags);
 
 /* Bytes of one routed-expert blob (codes + scales + biases, padded) and the
  * number of resident device bytes of the context (weights + workspace). */

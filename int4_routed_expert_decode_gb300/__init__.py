@@ -27,13 +27,14 @@ MOE_ERR_TIMEOUT = -7
 MOE_ERR_UNSUPPORTED = -8
 
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_GENERAL, MOE_PATH_PREFILL = 0, 1, 2, 3
+MOE_TEST_BARRIER_TIMEOUT = 1
 
 # every symbol include/moe.h declares
 EXPORTS = (
     "moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
     "moe_read_expert", "moe_set_path", "moe_expert_blob_bytes", "moe_device_bytes",
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
-    "moe_route_static",
+    "moe_route_static", "moe_set_test_flags",
 )
 
 
@@ -78,6 +79,7 @@ def lib():
     L.moe_get_status.argtypes = [vp, vp]
     L.moe_read_expert.argtypes = [vp, i32] + [vp] * 9
     L.moe_set_path.argtypes = [vp, i32]
+    L.moe_set_test_flags.argtypes = [vp, i32]
     L.moe_expert_blob_bytes.argtypes = [vp]
     L.moe_expert_blob_bytes.restype = i64
     L.moe_device_bytes.argtypes = [vp]
@@ -92,7 +94,8 @@ def lib():
     L.moe_route_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     L.moe_route_static.restype = i32
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
-                 "moe_read_expert", "moe_set_path", "moe_last_launch_count"):
+                 "moe_read_expert", "moe_set_path", "moe_last_launch_count",
+                 "moe_set_test_flags"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -207,6 +210,10 @@ def moe_read_expert(ctx: int, slot: int, H: int, I: int, G: int) -> dict:
 
 def moe_set_path(ctx: int, path: int):
     _check(lib().moe_set_path(ctx, path), ctx)
+
+
+def moe_set_test_flags(ctx: int, flags: int):
+    _check(lib().moe_set_test_flags(ctx, flags), ctx)
 
 
 def moe_expert_blob_bytes(ctx: int) -> int:

@@ -288,6 +288,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_h = take(rows * maxI * 4);
   const uint64_t o_o = take(rows * d.H * 4);
   const uint64_t o_err = take(4);
+  const uint64_t o_bar = take(8);
   uint8_t* base = nullptr;
   cudaError_t e = cudaMalloc(&base, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace alloc");
@@ -311,8 +312,10 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.h = (float*)(base + o_h);
   c.ws.o = (float*)(base + o_o);
   c.err = (int32_t*)(base + o_err);
+  c.ws.bar = (unsigned long long*)(base + o_bar);
   c.max_T = max_T;
-  if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess) {
+  if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess ||
+      (e = prepare_fused_decode(c)) != cudaSuccess) {
     free_workspace(c);
     return cuda_fail(ctx, e, "kernel attributes");
   }
@@ -344,10 +347,19 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   cudaStream_t st = (cudaStream_t)stream;
   FwdArgs a{(const uint16_t*)x, T, expert_slot_table, (uint16_t*)y, topk_idx, topk_w, perm, offsets};
   int launches = 0;
-  cudaError_t e = launch_router(c, a, st, &launches);
-  if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
-  if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
-  if (e == cudaSuccess) e = launch_general_experts(c, a, st, &launches);
+  const bool fused_ok = T == 1 && fused_decode_supported(c);
+  if (c.path == MOE_PATH_DECODE && !fused_ok)
+    return set_msg(ctx, MOE_ERR_UNSUPPORTED,
+                   "the fused decode path needs T = 1 and supported sizes");
+  cudaError_t e;
+  if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE)) {
+    e = launch_fused_decode(c, a, st, &launches);
+  } else {
+    e = launch_router(c, a, st, &launches);
+    if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+    if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
+    if (e == cudaSuccess) e = launch_general_experts(c, a, st, &launches);
+  }
   c.last_launches = launches;
   if (e != cudaSuccess) return cuda_fail(ctx, e, "moe_forward launch");
   return MOE_OK;
@@ -364,6 +376,9 @@ int moe_get_status(moe_ctx* ctx, void* stream) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
   if (v != 0) {
     cudaMemset(ctx->c.err, 0, 4);
+    // a timed-out grid barrier leaves its counter off the multiple of the
+    // grid size that every barrier expects: start it afresh
+    if (ctx->c.ws.bar) cudaMemset(ctx->c.ws.bar, 0, 8);
     return set_msg(ctx, v, "device reported: %s", moe_status_string(v));
   }
   return MOE_OK;
@@ -421,6 +436,14 @@ int moe_set_path(moe_ctx* ctx, int path) {
   if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL)
     return set_msg(ctx, MOE_ERR_INVALID_ARG, "path=%d unknown", path);
   ctx->c.path = path;
+  return MOE_OK;
+}
+
+int moe_set_test_flags(moe_ctx* ctx, int flags) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (flags & ~MOE_TEST_BARRIER_TIMEOUT)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "unknown test flag %d", flags);
+  ctx->c.test_flags = flags;
   return MOE_OK;
 }
 

@@ -44,6 +44,7 @@ struct Workspace {
   int32_t* hist;      // [nblk][E]   per-block expert counts (large T)
   float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
   float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
+  unsigned long long* bar;  // grid-barrier arrival counter of the fused kernel (monotonic)
 };
 
 struct Ctx {
@@ -66,6 +67,8 @@ struct Ctx {
   int64_t ws_bytes = 0;
   Workspace ws{};
   int32_t* err = nullptr;             // sticky device error word
+  int fused_ctas = 0;                 // CTAs of the fused decode kernel (0: unavailable)
+  int test_flags = 0;                 // MOE_TEST_* hooks
   int last_launches = 0;
   char msg[512] = {0};
 };
@@ -96,6 +99,11 @@ struct FwdArgs {
 // moe_reserve so that moe_forward makes no such call (graph capture).
 cudaError_t prepare_router(const Ctx& c);
 cudaError_t prepare_general_experts(const Ctx& c);
+
+// Fused single-launch decode (T = 1): availability, one-time set-up, launch.
+bool fused_decode_supported(const Ctx& c);
+cudaError_t prepare_fused_decode(Ctx& c);
+cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 
 cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);

@@ -244,3 +244,143 @@ def test_prefill_zipf_workload_sampled_rows():
     rows = sorted(rows.tolist() + [0, wl.T - 1])
     ref = O.moe_block(x, W, wl.k, wl.G, tokens=rows)
     U.assert_parity(out, ref, rows=rows, what="prefill")
+
+
+# ------------------------------------------------------------------ fused single-launch decode
+@pytest.mark.parametrize("wid", [0, 1, 2])
+def test_fused_decode_matches_oracle(wid):
+    wl = synth.WORKLOADS[wid]
+    W = _weights(wl, layer=3)
+    L = U.layer(wl.shape, W, max_T=1)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+    for step in range(4):
+        x = _x(wl, 1, layer=3, step=step)
+        out = U.run(L, x)
+        assert moe.moe_last_launch_count(L.ctx) == 1
+        ref = O.moe_block(x, W, wl.k, wl.G)
+        U.assert_parity(out, ref, what=f"fused wl{wid} step{step}")
+
+
+@pytest.mark.parametrize("wid", [0, 2])
+def test_fused_decode_agrees_with_general_path(wid):
+    wl = synth.WORKLOADS[wid]
+    W = _weights(wl, layer=5)
+    Lf = U.layer(wl.shape, W, max_T=1)
+    Lg = U.layer(wl.shape, W, max_T=1)
+    moe.moe_set_path(Lf.ctx, moe.MOE_PATH_DECODE)
+    moe.moe_set_path(Lg.ctx, moe.MOE_PATH_GENERAL)
+    for step in range(3):
+        x = _x(wl, 1, layer=5, step=step)
+        a, b = U.run(Lf, x), U.run(Lg, x)
+        for key in ("topk_idx", "perm", "offsets"):
+            assert np.array_equal(a[key], b[key]), key
+        assert np.max(np.abs(a["topk_w"] - b["topk_w"])) <= U.W_ABS
+        U.assert_y_close(a["y"], b["y"], what="fused vs general")
+
+
+def test_fused_decode_other_shapes():
+    """Group 128, hidden 1024, E = 64 (list length 8), larger k."""
+    for shape in (synth.Shape(E=64, k=6, H=1024, I=256, Is=256, G=128),
+                  synth.Shape(E=300, k=12, H=512, I=128, Is=128, G=32)):
+        W = synth.layer_weights(0, 0, 21, shape, zipf_s=0.5)
+        L = U.layer(shape, W, max_T=1)
+        moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+        for step in range(3):
+            x = synth.tokens(0, 0, 21, step, 1, shape.H)
+            U.assert_parity(U.run(L, x), O.moe_block(x, W, shape.k, shape.G),
+                            what=f"fused {shape} step{step}")
+
+
+def test_fused_decode_ties_and_near_ties():
+    W = _weights(W0)
+    rw = W["router_w"].copy()
+    rw[3] = rw[9]
+    rw[5] = rw[9]
+    rw[7] = rw[9]
+    rw[7, 11] ^= 1
+    W["router_w"] = rw
+    L = U.layer(W0.shape, W, max_T=1)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+    for step in range(6):
+        x = _x(W0, 1, step=step)
+        U.assert_parity(U.run(L, x), O.moe_block(x, W, W0.k, W0.G), what=f"ties step{step}")
+    W["router_w"] = np.repeat(W["router_w"][:1], W0.E, axis=0)
+    L2 = U.layer(W0.shape, W, max_T=1)
+    out = U.run(L2, _x(W0, 1))
+    assert out["topk_idx"].tolist() == [list(range(W0.k))]
+
+
+def test_fused_decode_placement_invariance():
+    wl = synth.WORKLOADS[1]
+    W = _weights(wl, layer=2)
+    x = _x(wl, 1, layer=2)
+    a = U.run(U.layer(wl.shape, W, max_T=1), x)
+    order = np.random.default_rng(3).permutation(wl.E)
+    Wp = dict(W)
+    Wp["experts"] = {k: np.ascontiguousarray(v[order]) for k, v in W["experts"].items()}
+    table = np.empty(wl.E, np.int32)
+    table[order] = np.arange(wl.E, dtype=np.int32)
+    b = U.run(U.layer(wl.shape, Wp, max_T=1), x, table=table)
+    for key in ("y_bits", "topk_idx", "topk_w", "perm", "offsets"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_fused_decode_missing_slot_reported():
+    W = _weights(W0)
+    L = U.layer(W0.shape, W, max_T=1)
+    x = _x(W0, 1)
+    out = U.run(L, x, table=np.full(W0.E, -1, np.int32))
+    assert out["status"] == moe.MOE_ERR_SLOT
+    assert U.run(L, x)["status"] == moe.MOE_OK
+
+
+def test_fused_decode_bounded_barrier_wait_reports_timeout():
+    """A barrier that waits for one CTA too many runs out (about a second); the
+    status says so and the context keeps working."""
+    W = _weights(W0)
+    L = U.layer(W0.shape, W, max_T=1)
+    x = _x(W0, 1)
+    moe.moe_set_test_flags(L.ctx, moe.MOE_TEST_BARRIER_TIMEOUT)
+    out = U.run(L, x)
+    assert out["status"] == moe.MOE_ERR_TIMEOUT
+    moe.moe_set_test_flags(L.ctx, 0)
+    out = U.run(L, x)
+    assert out["status"] == moe.MOE_OK
+    U.assert_parity(out, O.moe_block(x, W, W0.k, W0.G), what="after timeout")
+
+
+def test_fused_decode_graph_replay_of_stacked_layers():
+    """Several layers captured in one CUDA graph (programmatic dependent
+    launches between them) give the eager results on every replay."""
+    import torch
+    wl = synth.WORKLOADS[1]
+    nl = 3
+    Ws = [_weights(wl, layer=l) for l in range(nl)]
+    Ls = [U.layer(wl.shape, W, max_T=1) for W in Ws]
+    xs = [torch.from_numpy(_x(wl, 1, layer=l, step=7).view(np.int16)).cuda().view(torch.bfloat16)
+          for l in range(nl)]
+    ys = [torch.empty((1, wl.H), dtype=torch.bfloat16, device="cuda") for _ in range(nl)]
+    idx = [torch.empty((1, wl.k), dtype=torch.int32, device="cuda") for _ in range(nl)]
+    ws = [torch.empty((1, wl.k), dtype=torch.float32, device="cuda") for _ in range(nl)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for l in range(nl):
+            moe.moe_forward(Ls[l].ctx, xs[l], 1, None, ys[l], idx[l], ws[l], stream=s)
+    s.synchronize()
+    eager = [y.clone() for y in ys]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for l in range(nl):
+            moe.moe_forward(Ls[l].ctx, xs[l], 1, None, ys[l], idx[l], ws[l], stream=s)
+    for _ in range(5):
+        for y in ys:
+            y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(nl):
+            assert torch.equal(ys[l], eager[l])
+    for l in range(nl):
+        assert Ls[l].status() == moe.MOE_OK
+        ref = O.moe_block(_x(wl, 1, layer=l, step=7), Ws[l], wl.k, wl.G)
+        assert idx[l].cpu().numpy().tolist() == ref["topk_idx"].tolist()
+        U.assert_y_close(U.to_f64_bf16(ys[l]), ref["y"], what=f"graph layer {l}")
