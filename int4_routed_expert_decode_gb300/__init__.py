@@ -27,7 +27,7 @@ MOE_ERR_TIMEOUT = -7
 MOE_ERR_UNSUPPORTED = -8
 
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_GENERAL, MOE_PATH_PREFILL = 0, 1, 2, 3
-MOE_TEST_BARRIER_TIMEOUT = 1
+MOE_TEST_WAIT_TIMEOUT = 1
 
 # every symbol include/moe.h declares
 EXPORTS = (

@@ -44,7 +44,8 @@ struct Workspace {
   int32_t* hist;      // [nblk][E]   per-block expert counts (large T)
   float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
   float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
-  unsigned long long* bar;  // grid-barrier arrival counter of the fused kernel (monotonic)
+  unsigned long long* bar;  // fused kernel: [0] CTAs done, [1] epoch of the tagged words
+  unsigned long long* tg;   // fused kernel: tagged words (value | epoch << 32)
 };
 
 struct Ctx {
@@ -102,6 +103,8 @@ cudaError_t prepare_general_experts(const Ctx& c);
 
 // Fused single-launch decode (T = 1): availability, one-time set-up, launch.
 bool fused_decode_supported(const Ctx& c);
+int tagged_h_index(int E);
+int64_t tagged_words(const Dims& d);
 cudaError_t prepare_fused_decode(Ctx& c);
 cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 

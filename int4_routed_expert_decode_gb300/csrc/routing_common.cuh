@@ -246,58 +246,32 @@ static __device__ __forceinline__ void swap_sel(int* sel_idx, float* sel_val, ui
   __syncwarp();
 }
 
-// The k experts of one token in exact order, by one warp.
-//   lrow, brow: the token's E fp32 logits and bounds (global memory, read via L2)
-//   xt: the token's bf16 x (global); router_w, prior: router weights and prior
-//   smem: topk_warp_smem(E) bytes of this warp's shared memory
-// On return sel_idx[0..k) / sel_val[0..k) (inside smem) hold the experts in
-// descending exact logit (ties to the lower id) and their fp32 logits.
-//
-// Lane l holds experts l*MAXV .. l*MAXV + MAXV-1 (E <= 32*MAXV), sorted best
-// first.  Extraction repeatedly takes the best head over the warp (two warp
-// reductions per expert) until k are taken and the gap to the next exceeds
-// 2*beta, beta = the largest bound of the token; every run of neighbours
-// closer than 2*beta is then reordered by exact values.  Runs are bounded by
-// gaps > 2*beta, so exact values never cross a run boundary, and experts left
-// behind are beaten by k taken ones.
-template <int MAXV>
-__device__ void topk_select_warp(const float* lrow, const float* brow, int E, int k,
-                                 const uint16_t* xt, const uint16_t* router_w,
-                                 const float* prior, int H, uint8_t* smem, int** sel_idx_out,
-                                 float** sel_val_out) {
+// Take entries best first from per-lane sorted lists (key 0 = empty), one per
+// iteration, writing sel_idx/sel_val[n] (lane 0).  Stops after `limit`
+// entries, when the lists run dry (*closed = 2), or -- if close_on_gap -- once
+// n >= k and the next entry is more than thr below the last one taken
+// (*closed = 1).  Returns n.
+template <int N>
+__device__ int extract_sorted(uint32_t (&key)[N], int (&id)[N], int k, int limit, float thr,
+                              bool close_on_gap, int* sel_idx, float* sel_val, int* closed) {
   const int lane = threadIdx.x & 31;
-  int* sel_idx = reinterpret_cast<int*>(smem);
-  float* sel_val = reinterpret_cast<float*>(smem + (size_t)E * 4);
-  uint32_t* cache = reinterpret_cast<uint32_t*>(smem + (size_t)E * 8);
-  uint32_t* scratch = cache + kRunCache * kDigits;
-  *sel_idx_out = sel_idx;
-  *sel_val_out = sel_val;
-
-  uint32_t key[MAXV];
-  int id[MAXV];
-  uint32_t bmax = 0;  // bounds are non-negative: their bits order like the values
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int e = lane * MAXV + i;
-    float l = (e < E) ? __ldcg(lrow + e) : 0.f;
-    if (l != l) l = -INFINITY;  // a NaN logit from bad input ranks as -inf
-    key[i] = (e < E) ? f32_key(l) : 0u;  // key 0: empty (below every real logit)
-    id[i] = (e < E) ? e : 0x7FFFFFFF;
-    if (e < E) bmax = max(bmax, __float_as_uint(__ldcg(brow + e)));
-  }
-  const float thr = 2.0f * __uint_as_float(__reduce_max_sync(0xffffffffu, bmax));
-  sort_lane_desc<MAXV>(key, id);
-
   int n = 0;
-  while (n < E) {
+  *closed = 0;
+  while (n < limit) {
     const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[0]);
-    if (kmax == 0u) break;  // nothing left
+    if (kmax == 0u) {
+      *closed = 2;
+      break;
+    }
     const uint32_t win =
         __reduce_min_sync(0xffffffffu, key[0] == kmax ? (uint32_t)id[0] : 0xFFFFFFFFu);
     const float wv = key_f32(kmax);
-    if (n >= k) {
+    if (close_on_gap && n >= k) {
       const float last = sel_val[n - 1];
-      if (!(last - wv <= thr)) break;  // certified gap: the selection is closed
+      if (!(last - wv <= thr)) {  // certified gap: the selection is closed
+        *closed = 1;
+        break;
+      }
     }
     if (lane == 0) {
       sel_idx[n] = (int)win;
@@ -305,18 +279,28 @@ __device__ void topk_select_warp(const float* lrow, const float* brow, int E, in
     }
     if (key[0] == kmax && id[0] == (int)win) {  // pop this lane's head
 #pragma unroll
-      for (int i = 0; i < MAXV - 1; ++i) {
+      for (int i = 0; i < N - 1; ++i) {
         key[i] = key[i + 1];
         id[i] = id[i + 1];
       }
-      key[MAXV - 1] = 0u;
-      id[MAXV - 1] = 0x7FFFFFFF;
+      key[N - 1] = 0u;
+      id[N - 1] = 0x7FFFFFFF;
     }
     __syncwarp();
     ++n;
   }
   __syncwarp();
+  return n;
+}
 
+// Reorder, by exact values, every run of neighbours of sel[0..n) closer than
+// thr that reaches into the first k positions (one warp).  cache/scratch:
+// kRunCache*kDigits and 2*kDigits words of this warp's shared memory.
+static __device__ void resolve_runs(int* sel_idx, float* sel_val, int n, int k, float thr,
+                                    const uint16_t* xt, const uint16_t* router_w,
+                                    const float* prior, int H, uint32_t* cache,
+                                    uint32_t* scratch) {
+  const int lane = threadIdx.x & 31;
   int a = 0;
   while (a < n - 1 && a < k) {
     int b = a;
@@ -357,6 +341,71 @@ __device__ void topk_select_warp(const float* lrow, const float* brow, int E, in
     a = b + 1;
   }
   __syncwarp();
+}
+
+// Plain fp32 logits and bounds in global memory (read through L2).
+struct PlainLogits {
+  const float* l;
+  const float* b;
+  __device__ __forceinline__ void get(int e, float& logit, float& bnd) const {
+    logit = __ldcg(l + e);
+    bnd = __ldcg(b + e);
+  }
+};
+
+// The k experts of one token in exact order, by one warp.
+//   src: the token's E fp32 logits and their bounds (src.get(e, logit, bound))
+//   xt: the token's bf16 x (global); router_w, prior: router weights and prior
+//   smem: topk_warp_smem(E) bytes of this warp's shared memory
+// On return sel_idx[0..k) / sel_val[0..k) (inside smem) hold the experts in
+// descending exact logit (ties to the lower id) and their fp32 logits.
+//
+// Lane l holds experts l*MAXV .. l*MAXV + MAXV-1 (E <= 32*MAXV), sorted best
+// first.  Extraction repeatedly takes the best head over the warp (two warp
+// reductions per expert) until k are taken and the gap to the next exceeds
+// 2*beta, beta = the largest bound of the token; every run of neighbours
+// closer than 2*beta is then reordered by exact values.  Runs are bounded by
+// gaps > 2*beta, so exact values never cross a run boundary, and experts left
+// behind are beaten by k taken ones.
+template <int MAXV, typename Src>
+__device__ void topk_select_warp_src(const Src& src, int E, int k, const uint16_t* xt,
+                                     const uint16_t* router_w, const float* prior, int H,
+                                     uint8_t* smem, int** sel_idx_out, float** sel_val_out) {
+  const int lane = threadIdx.x & 31;
+  int* sel_idx = reinterpret_cast<int*>(smem);
+  float* sel_val = reinterpret_cast<float*>(smem + (size_t)E * 4);
+  uint32_t* cache = reinterpret_cast<uint32_t*>(smem + (size_t)E * 8);
+  uint32_t* scratch = cache + kRunCache * kDigits;
+  *sel_idx_out = sel_idx;
+  *sel_val_out = sel_val;
+
+  uint32_t key[MAXV];
+  int id[MAXV];
+  uint32_t bmax = 0;  // bounds are non-negative: their bits order like the values
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int e = lane * MAXV + i;
+    float l = 0.f, bnd = 0.f;
+    if (e < E) src.get(e, l, bnd);
+    if (l != l) l = -INFINITY;  // a NaN logit from bad input ranks as -inf
+    key[i] = (e < E) ? f32_key(l) : 0u;  // key 0: empty (below every real logit)
+    id[i] = (e < E) ? e : 0x7FFFFFFF;
+    if (e < E) bmax = max(bmax, __float_as_uint(bnd));
+  }
+  const float thr = 2.0f * __uint_as_float(__reduce_max_sync(0xffffffffu, bmax));
+  sort_lane_desc<MAXV>(key, id);
+  int closed;
+  const int n = extract_sorted<MAXV>(key, id, k, E, thr, true, sel_idx, sel_val, &closed);
+  resolve_runs(sel_idx, sel_val, n, k, thr, xt, router_w, prior, H, cache, scratch);
+}
+
+template <int MAXV>
+__device__ void topk_select_warp(const float* lrow, const float* brow, int E, int k,
+                                 const uint16_t* xt, const uint16_t* router_w,
+                                 const float* prior, int H, uint8_t* smem, int** sel_idx_out,
+                                 float** sel_val_out) {
+  topk_select_warp_src<MAXV>(PlainLogits{lrow, brow}, E, k, xt, router_w, prior, H, smem,
+                             sel_idx_out, sel_val_out);
 }
 
 // Renormalised softmax weight of selected expert `lane` (lanes < k), i.e.

@@ -334,13 +334,13 @@ def test_fused_decode_missing_slot_reported():
     assert U.run(L, x)["status"] == moe.MOE_OK
 
 
-def test_fused_decode_bounded_barrier_wait_reports_timeout():
-    """A barrier that waits for one CTA too many runs out (about a second); the
-    status says so and the context keeps working."""
+def test_fused_decode_bounded_wait_reports_timeout():
+    """Waits for data stamped with an epoch nobody writes run out (about a
+    second each); the status says so and the context keeps working."""
     W = _weights(W0)
     L = U.layer(W0.shape, W, max_T=1)
     x = _x(W0, 1)
-    moe.moe_set_test_flags(L.ctx, moe.MOE_TEST_BARRIER_TIMEOUT)
+    moe.moe_set_test_flags(L.ctx, moe.MOE_TEST_WAIT_TIMEOUT)
     out = U.run(L, x)
     assert out["status"] == moe.MOE_ERR_TIMEOUT
     moe.moe_set_test_flags(L.ctx, 0)
