@@ -155,11 +155,12 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
 enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_GENERAL = 2, MOE_PATH_PREFILL = 3 };
 int moe_set_path(moe_ctx* ctx, int path);
 
-/* Test hooks, off by default.  MOE_TEST_WAIT_TIMEOUT makes the fused decode
- * kernel wait for data stamped with an epoch that no CTA writes: every
- * bounded wait runs out (about one second each), the device records
- * MOE_ERR_TIMEOUT, and moe_get_status reports it and resets the epoch so
- * that the context stays usable.  flags = 0 turns every hook off. */
+/* Test hooks, off by default.  MOE_TEST_WAIT_TIMEOUT makes the grid
+ * barriers of the fused decode kernel wait for one arrival more than the
+ * grid has: each bounded wait runs out (about one second), the device
+ * records MOE_ERR_TIMEOUT, and moe_get_status reports it and resets the
+ * barrier counter so that the context stays usable.  flags = 0 turns every
+ * hook off. */
 enum { MOE_TEST_WAIT_TIMEOUT = 1 };
 int moe_set_test_flags(moe_ctx* ctx, int flags);
 

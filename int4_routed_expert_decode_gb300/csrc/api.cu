@@ -288,8 +288,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_h = take(rows * maxI * 4);
   const uint64_t o_o = take(rows * d.H * 4);
   const uint64_t o_err = take(4);
-  const uint64_t o_bar = take(16);
-  const uint64_t o_tg = take((uint64_t)tagged_words(d) * 8);
+  const uint64_t o_bar = take(kSyncWords * 8);
   uint8_t* base = nullptr;
   cudaError_t e = cudaMalloc(&base, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace alloc");
@@ -314,7 +313,6 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.o = (float*)(base + o_o);
   c.err = (int32_t*)(base + o_err);
   c.ws.bar = (unsigned long long*)(base + o_bar);
-  c.ws.tg = (unsigned long long*)(base + o_tg);
   c.max_T = max_T;
   if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess ||
       (e = prepare_fused_decode(c)) != cudaSuccess) {
@@ -378,9 +376,9 @@ int moe_get_status(moe_ctx* ctx, void* stream) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
   if (v != 0) {
     cudaMemset(ctx->c.err, 0, 4);
-    // after an error start the fused kernel's epoch and tagged words afresh
-    if (ctx->c.ws.bar) cudaMemset(ctx->c.ws.bar, 0, 16);
-    if (ctx->c.ws.tg) cudaMemset(ctx->c.ws.tg, 0, (size_t)tagged_words(ctx->c.d) * 8);
+    // a timed-out grid barrier leaves its counter off the multiple of the
+    // grid size that every barrier expects: start it afresh
+    if (ctx->c.ws.bar) cudaMemset(ctx->c.ws.bar, 0, kSyncWords * 8);
     return set_msg(ctx, v, "device reported: %s", moe_status_string(v));
   }
   return MOE_OK;

@@ -2,7 +2,8 @@
 //
 // Decode moves ~17-22 MB of int4 expert weights per layer and token, so it is
 // bound by HBM bandwidth and by latency, not by arithmetic.  One persistent
-// CTA per SM runs the block in four phases:
+// CTA per SM runs the block in four phases separated by two bounded grid
+// barriers:
 //
 //   P0  before waiting on the previous kernel (programmatic dependent launch):
 //       bulk-copy (TMA, 1-D) this CTA's slice of the router rows, of the shared
@@ -10,29 +11,22 @@
 //       are weights and do not depend on earlier kernels;
 //   P1  router logits with their rigorous error bounds, and the shared
 //       expert's gate/up + SwiGLU (neither depends on routing);
-//   P2  every CTA selects the top-k itself (exact order, routing_common.cuh):
-//       each warp takes the best k+8 of its eighth of the experts, warp 0
-//       merges them; then bulk-copies its share of the selected experts'
-//       gate/up rows and its rows of their down projections;
+//       -- grid barrier --
+//   P2  every CTA selects the top-k itself (exact order, routing_common.cuh),
+//       then bulk-copies its share of the selected experts' gate/up rows and
+//       its rows of their down projections;
 //   P3  gate/up + SwiGLU of the selected experts from shared memory;
+//       -- grid barrier --
 //   P4  this CTA's rows of y: sum_j w_j (Wd_j h_j) + g (Wd_s h_s), fixed order
 //       (deterministic), bf16 out.
-//
-// No grid barrier: the values that cross CTAs (logits, bounds, the shared
-// gate, h) are stored as 64-bit words (value | epoch << 32).  A reader polls
-// just the words it needs until they carry this launch's epoch, so it waits
-// for its own producers only, one L2 round trip after they wrote.  The last
-// CTA to finish advances the epoch; the next launch reads it after
-// griddepcontrol.wait, when every CTA of this one has finished.  Polls are
-// bounded (one second); on expiry the sticky error word gets MOE_ERR_TIMEOUT.
 //
 // The int4 dot products fold the affine terms per 32-code chunk, with the
 // codes turned into floats 1 + q/128 by one byte-permute each:
 //   sum_c (s q_c + b) x_c = (128 s) * sum_c (1 + q_c/128) x_c + (b - 128 s) * sum_c x_c,
 // two codes per packed fp32 FMA (FFMA2).  Each lane keeps the inputs of its
-// own chunks (x, or h in P4) in registers.  Weights follow the MLX affine
-// int4 group layout (Swiftlet README, "MLX affine int4/int8 group
-// quantization").
+// own chunks (x, or h in P4) in registers, read once from global memory.
+// Weights follow the MLX affine int4 group layout (Swiftlet README, "MLX
+// affine int4/int8 group quantization").
 #include "device_util.cuh"
 #include "moe_internal.cuh"
 #include "routing_common.cuh"
@@ -46,13 +40,12 @@ using namespace rt;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
-constexpr int kExtra = 8;                  // candidates per warp beyond k in the top-k
-constexpr uint32_t kPollSpin = 1u << 22;   // polls per wait (with sleeps and a 1 s limit)
+constexpr uint32_t kBarSpin = 1u << 22;    // grid-barrier polls (with sleeps and a 1 s limit)
 constexpr uint32_t kMbarTries = 1u << 22;  // mbarrier try_waits
 constexpr int kNumMbar = 10;               // 0: P0 weights, 1..8: P3 warps, 9: P4 down rows
 
 struct FusedSmem {  // byte offsets into dynamic shared memory
-  uint32_t mbar, misc, topk, cand, p1, sd, p3, p3_warp, p4, p4_expert, p4_sb, ypart, total;
+  uint32_t mbar, misc, topk, p1, sd, p3, p3_warp, p4, p4_expert, p4_sb, ypart, total;
   uint32_t p1_max;    // bytes reserved for router + shared gate/up rows
   uint32_t seg_max;   // row-pairs per warp segment (max)
   uint32_t nrow_max;  // P4 rows per CTA (max)
@@ -74,12 +67,15 @@ struct FusedArgs {
   float* topk_w;
   int32_t* perm_out;
   int32_t* offsets_out;
-  unsigned long long* tg;    // tagged words: logits [E], bounds [E], gate, h [k][I], hs [I]
-  int tg_h;                  // index of h in tg (even: 16-byte aligned)
-  unsigned long long* sync;  // [0] CTAs done, [1] epoch
-  uint32_t tag_extra;        // test hook: readers wait for an epoch nobody writes
+  float* logits;
+  float* bound;
+  float* gate_z;
+  float* h;   // [k][I]
+  float* hs;  // [I]
+  unsigned long long* bar;
+  uint32_t bar_extra;  // test hook: arrivals the barrier waits for beyond the grid
   int32_t* err;
-  int E, k, I, G, gshift;
+  int E, k, I, G;
   FusedSmem sm;
 };
 
@@ -87,26 +83,30 @@ __device__ __forceinline__ int part(int n, int parts, int p) {
   return (int)(((long long)n * p) / parts);
 }
 
-__device__ __forceinline__ unsigned long long tagged(float v, uint32_t tag) {
-  return (unsigned long long)__float_as_uint(v) | ((unsigned long long)tag << 32);
-}
-__device__ __forceinline__ uint32_t tag_of(unsigned long long w) { return (uint32_t)(w >> 32); }
-__device__ __forceinline__ float val_of(unsigned long long w) { return __uint_as_float((uint32_t)w); }
-
-// Bounded poll: true while the caller should keep waiting.
-struct Poll {
-  uint64_t t0 = 0;
-  uint32_t it = 0;
-  __device__ __forceinline__ bool again(int32_t* err) {
-    if (it == 0) t0 = ptx::globaltimer_ns();
-    if (++it > kPollSpin || ptx::globaltimer_ns() - t0 > 1000000000ull) {
-      record_error(err, MOE_ERR_TIMEOUT);
-      return false;
+// Grid-wide barrier on a monotonic 64-bit arrival counter: barrier number b
+// (counting from the last reset) is passed once the counter reaches
+// (b + 1) * n, so one atomic round trip per CTA suffices.  Polls stop after
+// kBarSpin tries or one second; on expiry the sticky error word gets
+// MOE_ERR_TIMEOUT and the CTA carries on (no trap, no hang).
+__device__ void grid_barrier(unsigned long long* bar, uint32_t n, int32_t* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long old = ptx::atom_add_acq_rel_u64(bar, 1ull);
+    const unsigned long long target = (old / n + 1) * n;
+    if (old + 1 < target) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      uint32_t it = 0;
+      while (ptx::ld_acquire_u64(bar) < target) {
+        if (++it > kBarSpin || ptx::globaltimer_ns() - t0 > 1000000000ull) {
+          record_error(err, MOE_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
     }
-    __nanosleep(64);
-    return true;
   }
-};
+  __syncthreads();
+}
 
 __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, int32_t* err) {
   if (!ptx::mbar_wait(bar, parity, kMbarTries)) record_error(err, MOE_ERR_TIMEOUT);
@@ -114,7 +114,7 @@ __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, int
 
 // sum_i (1 + q_i/128) x_i over the 32 codes of a chunk; x as 16 float2.
 __device__ __forceinline__ float dot32_magic(uint4 w, const float2 (&x2)[16]) {
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  float2 acc = make_float2(0.f, 0.f);
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -124,13 +124,10 @@ __device__ __forceinline__ float dot32_magic(uint4 w, const float2 (&x2)[16]) {
     for (int b = 0; b < 4; ++b) {
       const float f0 = __uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044u | (b << 8)));
       const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044u | (b << 8)));
-      if (b & 1)
-        acc1 = __ffma2_rn(make_float2(f0, f1), x2[4 * j + b], acc1);
-      else
-        acc0 = __ffma2_rn(make_float2(f0, f1), x2[4 * j + b], acc0);
+      acc = __ffma2_rn(make_float2(f0, f1), x2[4 * j + b], acc);
     }
   }
-  return (acc0.x + acc1.x) + (acc0.y + acc1.y);
+  return acc.x + acc.y;
 }
 
 // Contribution of one 32-code chunk with packed (scale | bias << 16) and the
@@ -158,37 +155,19 @@ __device__ __forceinline__ float load_chunk_bf16(const uint16_t* src, float2 (&v
   return s;
 }
 
-// 32 consecutive tagged words once they all carry `want`, as 16 float2, and
-// their sum.  False (and the error word set) if the bounded poll ran out.
-__device__ __forceinline__ float poll_chunk_tagged(const unsigned long long* src, uint32_t want,
-                                                   float2 (&v)[16], int32_t* err) {
-  const ulonglong2* p = reinterpret_cast<const ulonglong2*>(src);
-  Poll poll;
-  while (true) {
-    bool ok = true;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const ulonglong2 u = __ldcg(p + q);
-      ok &= (tag_of(u.x) == want) & (tag_of(u.y) == want);
-      v[q] = make_float2(val_of(u.x), val_of(u.y));
-    }
-    if (ok || !poll.again(err)) break;
-  }
+// 32 consecutive fp32 written earlier in this kernel (read through L2).
+__device__ __forceinline__ float load_chunk_f32(const float* src, float2 (&v)[16]) {
+  const float4* p = reinterpret_cast<const float4*>(src);
   float s = 0.f;
 #pragma unroll
-  for (int q = 0; q < 16; ++q) s += v[q].x + v[q].y;
+  for (int q = 0; q < 8; ++q) {
+    const float4 u = __ldcg(p + q);
+    v[2 * q] = make_float2(u.x, u.y);
+    v[2 * q + 1] = make_float2(u.z, u.w);
+    s += (u.x + u.y) + (u.z + u.w);
+  }
   return s;
 }
-
-// Tagged fp32 logits and bounds (all complete when read).
-struct TaggedLogits {
-  const unsigned long long* tg;
-  int E;
-  __device__ __forceinline__ void get(int e, float& logit, float& bnd) const {
-    logit = val_of(__ldcg(tg + e));
-    bnd = val_of(__ldcg(tg + E + e));
-  }
-};
 
 // A 16-byte aligned window [lo, hi) around bytes [b0, b1) of a region whose
 // size is a multiple of 16: returns lo and the padded length.
@@ -198,37 +177,22 @@ __device__ __forceinline__ void align16(uint64_t b0, uint64_t b1, uint64_t& lo, 
   len = (uint32_t)(hi - lo);
 }
 
-// Sum over groups of `width` lanes of four values at once.
-__device__ __forceinline__ void group_sum4(float& a, float& b, float& c, float& d, int width) {
-  for (int o = width >> 1; o > 0; o >>= 1) {
-    a += __shfl_xor_sync(0xffffffffu, a, o);
-    b += __shfl_xor_sync(0xffffffffu, b, o);
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-    d += __shfl_xor_sync(0xffffffffu, d, o);
-  }
-}
-
 template <int NJ, int MAXV>
 __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedArgs a) {
   constexpr int H = NJ * 256;
   constexpr int HC = H / 32;          // 32-code chunks per gate/up row
   constexpr int MC = (HC + 31) / 32;  // chunks per lane
-  constexpr int MW = MAXV / 8;        // experts per lane in a warp's eighth
-  constexpr int MM = 16;              // merge candidates per lane (8 warps x (k+8) <= 512)
   extern __shared__ __align__(1024) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nC = gridDim.x, c = blockIdx.x;
-  const int E = a.E, k = a.k, I = a.I, gs = a.gshift;
-  const int HG = H >> gs, IG = I >> gs, IC = I / 32;
+  const int E = a.E, k = a.k, I = a.I, G = a.G;
+  const int HG = H / G, IG = I / G, IC = I / 32;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.sm.mbar);
   int* s_idx = reinterpret_cast<int*>(sm + a.sm.misc);
   float* s_w = reinterpret_cast<float*>(sm + a.sm.misc + 128);
   int* s_slot = reinterpret_cast<int*>(sm + a.sm.misc + 256);
   float* s_g = reinterpret_cast<float*>(sm + a.sm.misc + 384);
-  uint32_t* s_tag = reinterpret_cast<uint32_t*>(sm + a.sm.misc + 388);
   float* ypart = reinterpret_cast<float*>(sm + a.sm.ypart);
-  unsigned long long* tg = a.tg;
-  unsigned long long* tg_h = a.tg + a.tg_h;  // [k][I] then the shared [I]
 
   // unit ranges of this CTA
   const int U1 = E + I + 1;  // router rows, shared features, gate vector
@@ -274,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   }
   // everything below may read what earlier kernels wrote
   ptx::griddep_wait();
-  if (threadIdx.x == 0) *s_tag = (uint32_t)(ptx::ld_acquire_u64(a.sync + 1) + 1);
 
   // x in registers: router layout (8 bf16 per uint4, chunks lane + 32 j) and
   // expert layout (32 fp32 per chunk, chunks lane + 32 m, with chunk sums)
@@ -288,9 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
     const int ch = lane + 32 * m;
     xs_r[m] = load_chunk_bf16(a.x + (ch < HC ? ch : 0) * 32, xr[m]);
   }
-  __syncthreads();
-  const uint32_t tag = *s_tag;
-  const uint32_t want = tag + a.tag_extra;
 
   // ---------------------------------------------------------------- P1
   wait_or_flag(&mbar[0], 0, a.err);
@@ -307,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
         if (u < E) {
           float l, b;
           router_logit_and_bound<NJ>(sum, mag, a.prior ? __ldg(a.prior + u) : 0.f, l, b);
-          tg[u] = tagged(l, tag);
-          tg[E + u] = tagged(b, tag);
+          a.logits[u] = l;
+          a.bound[u] = b;
         } else {
-          tg[2 * E] = tagged(sum, tag);
+          a.gate_z[0] = sum;
         }
       }
     } else {  // shared expert feature i: gate/up + SwiGLU
@@ -322,104 +282,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       for (int m = 0; m < MC; ++m) {
         const int ch = lane + 32 * m;
         if (ch < HC) {
-          const int g = (ch * 32) >> gs;
+          const int g = ch * 32 / G;
           ag += chunk_term(q4[ch], sb[g], xr[m], xs_r[m]);
           au += chunk_term(q4[HC + ch], sb[HG + g], xr[m], xs_r[m]);
         }
       }
       ag = warp_sum(ag);
       au = warp_sum(au);
-      if (lane == 0) tg_h[(size_t)k * I + i] = tagged(silu_f(ag) * au, tag);
+      if (lane == 0) a.hs[i] = silu_f(ag) * au;
     }
   }
+  grid_barrier(a.bar, nC + a.bar_extra, a.err);
 
   // ---------------------------------------------------------------- P2
-  {
-    // each warp: the best k + kExtra of its eighth of the experts
-    int* cand_idx = reinterpret_cast<int*>(sm + a.sm.cand);
-    float* cand_val = reinterpret_cast<float*>(sm + a.sm.cand + kWarps * (kMaxK + kExtra) * 4);
-    int* cand_n = reinterpret_cast<int*>(sm + a.sm.cand + 2 * kWarps * (kMaxK + kExtra) * 4);
-    uint32_t* cand_b = reinterpret_cast<uint32_t*>(cand_n + kWarps);
-    const int S = (E + kWarps - 1) / kWarps;
-    const int e0 = min(E, warp * S), e1 = min(E, e0 + S);
-    uint32_t key[MW];
-    int id[MW];
-    uint32_t bmax = 0;
-    Poll poll;
-    while (true) {
-      bool ok = true;
-      bmax = 0;
-#pragma unroll
-      for (int i = 0; i < MW; ++i) {
-        const int e = e0 + lane * MW + i;
-        key[i] = 0u;
-        id[i] = 0x7FFFFFFF;
-        if (e < e1) {
-          const unsigned long long lw = __ldcg(tg + e), bw = __ldcg(tg + E + e);
-          ok &= (tag_of(lw) == want) & (tag_of(bw) == want);
-          float l = val_of(lw);
-          if (l != l) l = -INFINITY;  // a NaN logit from bad input ranks as -inf
-          key[i] = f32_key(l);
-          id[i] = e;
-          bmax = max(bmax, __float_as_uint(val_of(bw)));
-        }
-      }
-      if (__all_sync(0xffffffffu, ok) || !poll.again(a.err)) break;
-    }
-    sort_lane_desc<MW>(key, id);
-    bmax = __reduce_max_sync(0xffffffffu, bmax);
-    int closed;
-    const int nw = extract_sorted<MW>(key, id, k, min(e1 - e0, k + kExtra), 0.f, false,
-                                      cand_idx + warp * (kMaxK + kExtra),
-                                      cand_val + warp * (kMaxK + kExtra), &closed);
-    if (lane == 0) {
-      cand_n[warp] = nw;
-      cand_b[warp] = bmax;
-    }
-  }
-  __syncthreads();
   if (warp == 0) {
-    int* cand_idx = reinterpret_cast<int*>(sm + a.sm.cand);
-    float* cand_val = reinterpret_cast<float*>(sm + a.sm.cand + kWarps * (kMaxK + kExtra) * 4);
-    int* cand_n = reinterpret_cast<int*>(sm + a.sm.cand + 2 * kWarps * (kMaxK + kExtra) * 4);
-    uint32_t* cand_b = reinterpret_cast<uint32_t*>(cand_n + kWarps);
-    uint8_t* tk = sm + a.sm.topk;
-    int* sel_idx = reinterpret_cast<int*>(tk);
-    float* sel_val = reinterpret_cast<float*>(tk + (size_t)E * 4);
-    uint32_t* cache = reinterpret_cast<uint32_t*>(tk + (size_t)E * 8);
-    uint32_t* scratch = cache + kRunCache * kDigits;
-    uint32_t bmax = 0;
-    bool truncated = false;
-    const int S = (E + kWarps - 1) / kWarps;
-    for (int w = 0; w < kWarps; ++w) {
-      bmax = max(bmax, cand_b[w]);
-      truncated |= (min(E, min(E, w * S) + S) - min(E, w * S)) > cand_n[w];
-    }
-    const float thr = 2.0f * __uint_as_float(bmax);
-    // merge: candidate slot q = lane * MM + i is entry (q % (k + kExtra)) of warp q / (k + kExtra)
-    const int per = k + kExtra;
-    uint32_t key[MM];
-    int id[MM];
-#pragma unroll
-    for (int i = 0; i < MM; ++i) {
-      const int q = lane * MM + i, w = q / per, j = q % per;
-      const bool have = w < kWarps && j < cand_n[w < kWarps ? w : 0];
-      key[i] = have ? f32_key(cand_val[w * (kMaxK + kExtra) + j]) : 0u;
-      id[i] = have ? cand_idx[w * (kMaxK + kExtra) + j] : 0x7FFFFFFF;
-    }
-    sort_lane_desc<MM>(key, id);
-    int closed;
-    int n = extract_sorted<MM>(key, id, k, min(E, per - 1), thr, true, sel_idx, sel_val, &closed);
-    if (closed == 1 || (closed == 2 && !truncated)) {
-      resolve_runs(sel_idx, sel_val, n, k, thr, a.x, a.router_w, a.prior, H, cache, scratch);
-    } else {
-      // the chain of near-equal logits runs past the merged candidates: the
-      // full single-warp selection over all E experts
-      int* si;
-      float* sv;
-      topk_select_warp_src<MAXV>(TaggedLogits{tg, E}, E, k, a.x, a.router_w, a.prior, H, tk,
-                                 &si, &sv);
-    }
+    int* sel_idx;
+    float* sel_val;
+    topk_select_warp<MAXV>(a.logits, a.bound, E, k, a.x, a.router_w, a.prior, H,
+                           sm + a.sm.topk, &sel_idx, &sel_val);
     const float w = renormalised_weight(sel_val, k);
     if (lane < k) {
       const int e = sel_idx[lane];
@@ -434,13 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
         a.topk_w[lane] = w;
       }
     }
-    if (lane == 0) {
-      unsigned long long gw;
-      Poll poll;
-      while (tag_of(gw = __ldcg(tg + 2 * E)) != want && poll.again(a.err)) {
-      }
-      *s_g = 1.0f / (1.0f + __expf(-val_of(gw)));
-    }
+    if (lane == 0) *s_g = 1.0f / (1.0f + __expf(-__ldcg(a.gate_z)));
   }
   __syncthreads();
 
@@ -506,42 +380,32 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   }
 
   // ---------------------------------------------------------------- P3
-  // two row-pairs per step: four independent dot products and reductions
   wait_or_flag(&mbar[1 + warp], 0, a.err);
-  for (int r = w0; r < w1; r += 2) {
-    const bool two = r + 1 < w1;
-    const int jA = r / I, iA = r % I;
-    const int jB = two ? (r + 1) / I : jA, iB = two ? (r + 1) % I : iA;
-    const bool okA = s_slot[jA] >= 0, okB = two && s_slot[jB] >= 0;
-    const uint4* qA = reinterpret_cast<const uint4*>(p3w + (size_t)(r - w0) * H);
-    const uint4* qB = reinterpret_cast<const uint4*>(p3w + (size_t)(r - w0 + (two ? 1 : 0)) * H);
-    const uint32_t* sbA = reinterpret_cast<const uint32_t*>(p3w_sb + (size_t)(r - w0) * rp_sb);
-    const uint32_t* sbB =
-        reinterpret_cast<const uint32_t*>(p3w_sb + (size_t)(r - w0 + (two ? 1 : 0)) * rp_sb);
-    float agA = 0.f, auA = 0.f, agB = 0.f, auB = 0.f;
+  for (int r = w0; r < w1; ++r) {
+    const int j = r / I, i = r % I;
+    if (s_slot[j] < 0) continue;
+    const uint4* q4 = reinterpret_cast<const uint4*>(p3w + (size_t)(r - w0) * H);
+    const uint32_t* sb = reinterpret_cast<const uint32_t*>(p3w_sb + (size_t)(r - w0) * rp_sb);
+    float ag = 0.f, au = 0.f;
 #pragma unroll
     for (int m = 0; m < MC; ++m) {
       const int ch = lane + 32 * m;
       if (ch < HC) {
-        const int g = (ch * 32) >> gs;
-        agA += chunk_term(qA[ch], sbA[g], xr[m], xs_r[m]);
-        auA += chunk_term(qA[HC + ch], sbA[HG + g], xr[m], xs_r[m]);
-        agB += chunk_term(qB[ch], sbB[g], xr[m], xs_r[m]);
-        auB += chunk_term(qB[HC + ch], sbB[HG + g], xr[m], xs_r[m]);
+        const int g = ch * 32 / G;
+        ag += chunk_term(q4[ch], sb[g], xr[m], xs_r[m]);
+        au += chunk_term(q4[HC + ch], sb[HG + g], xr[m], xs_r[m]);
       }
     }
-    group_sum4(agA, auA, agB, auB, 32);
-    if (lane == 0) {
-      if (okA) tg_h[(size_t)jA * I + iA] = tagged(silu_f(agA) * auA, tag);
-      if (okB) tg_h[(size_t)jB * I + iB] = tagged(silu_f(agB) * auB, tag);
-    }
+    ag = warp_sum(ag);
+    au = warp_sum(au);
+    if (lane == 0) a.h[(size_t)j * I + i] = silu_f(ag) * au;
   }
+  grid_barrier(a.bar, nC + a.bar_extra, a.err);
 
   // ---------------------------------------------------------------- P4
   // A group of `lpu` lanes owns one expert j (j == k: the shared one); lane
-  // `sub` holds chunk `sub` of h_j in registers and walks this CTA's rows,
-  // four at a time.  The trip counts depend on the warp only, so the group
-  // sums see every lane.
+  // `sub` holds chunk `sub` of h_j in registers and walks this CTA's rows.
+  // The trip counts depend on the warp only, so the group sums see every lane.
   wait_or_flag(&mbar[kNumMbar - 1], 0, a.err);
   {
     int lpu = 1;
@@ -555,33 +419,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       const bool valid = in_range && (shared || s_slot[j] >= 0) && sub < IC;
       float2 hr[16];
       float hsum = 0.f;
-      if (valid) hsum = poll_chunk_tagged(tg_h + (size_t)j * I + sub * 32, want, hr, a.err);
-      __syncwarp();
+      if (valid)
+        hsum = load_chunk_f32((shared ? a.hs : a.h + (size_t)j * I) + sub * 32, hr);
       const uint8_t* qbase =
           shared ? sd_q : sm + a.sm.p4 + (size_t)(in_range ? j : 0) * a.sm.p4_expert;
       const uint8_t* sbbase = shared ? sd_sb + dsb_off
                                      : sm + a.sm.p4 + (size_t)(in_range ? j : 0) * a.sm.p4_expert +
                                            a.sm.p4_sb + dsb_off;
-      const int gsub = (sub * 32) >> gs;
-      for (int rl = 0; rl < nrow; rl += 4) {
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int rl = 0; rl < nrow; ++rl) {
+        float v = 0.f;
         if (valid) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (rl + t < nrow) {
-              const uint4 q = reinterpret_cast<const uint4*>(qbase + (size_t)(rl + t) * (I / 2))[sub];
-              const uint32_t sbw =
-                  reinterpret_cast<const uint32_t*>(sbbase + (size_t)(rl + t) * IG * 4)[gsub];
-              v[t] = chunk_term(q, sbw, hr, hsum);
-            }
-          }
+          const uint4 q = reinterpret_cast<const uint4*>(qbase + (size_t)rl * (I / 2))[sub];
+          const uint32_t sbw =
+              reinterpret_cast<const uint32_t*>(sbbase + (size_t)rl * IG * 4)[sub * 32 / G];
+          v = chunk_term(q, sbw, hr, hsum);
         }
-        group_sum4(v[0], v[1], v[2], v[3], lpu);
-        if (in_range && sub == 0) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (rl + t < nrow) ypart[(rl + t) * (k + 1) + j] = v[t];
-        }
+        v = group_sum(v, lpu);
+        if (in_range && sub == 0) ypart[rl * (k + 1) + j] = v;
       }
     }
   }
@@ -592,16 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       if (s_slot[j] >= 0) acc = fmaf(s_w[j], ypart[rl * (k + 1) + j], acc);
     acc = fmaf(*s_g, ypart[rl * (k + 1) + k], acc);
     a.y[r0 + rl] = f32_to_bf16_rne(acc);
-  }
-
-  // the last CTA to finish advances the epoch for the next launch
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned long long done = ptx::atom_add_acq_rel_u64(a.sync, 1ull);
-    if (done == (unsigned long long)nC - 1) {
-      a.sync[0] = 0;
-      ptx::st_release_u64(a.sync + 1, (unsigned long long)tag);
-    }
   }
 }
 
@@ -619,7 +463,6 @@ bool plan_smem(const Ctx& c, int nC, FusedSmem& s) {
   s.mbar = take(kNumMbar * 8);
   s.misc = take(512);
   s.topk = take((uint32_t)topk_warp_smem(E));
-  s.cand = take(2 * kWarps * (kMaxK + kExtra) * 4 + 2 * kWarps * 4);
   // P1: worst CTA of router rows * 2H + shared features * (H + 8H/G)
   const int U1 = E + I + 1;
   uint32_t p1 = 0;
@@ -672,17 +515,6 @@ cudaError_t prepare_t(int smem, int* occ) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fused_decode_kernel<NJ, MAXV>,
                                                        kThreads, smem);
 }
-
-}  // namespace
-
-int tagged_h_index(int E) { return (2 * E + 1 + 1) & ~1; }
-
-int64_t tagged_words(const Dims& d) {
-  const int maxI = d.I > d.Is ? d.I : d.Is;
-  return (int64_t)tagged_h_index(d.E) + (int64_t)(d.k + 1) * maxI;
-}
-
-namespace {
 
 bool shape_ok(const Dims& d) {
   const int nj = d.H / 256;
@@ -758,16 +590,18 @@ cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& fa, cudaStream_t st
   a.topk_w = fa.topk_w;
   a.perm_out = fa.perm_out;
   a.offsets_out = fa.offsets_out;
-  a.tg = c.ws.tg;
-  a.tg_h = tagged_h_index(d.E);
-  a.sync = c.ws.bar;
-  a.tag_extra = (c.test_flags & MOE_TEST_WAIT_TIMEOUT) ? 1u : 0u;
+  a.logits = c.ws.logits;
+  a.bound = c.ws.bound;
+  a.gate_z = c.ws.gate_z;
+  a.h = c.ws.h;
+  a.hs = c.ws.h + (size_t)d.k * d.I;
+  a.bar = c.ws.bar;
+  a.bar_extra = (c.test_flags & MOE_TEST_WAIT_TIMEOUT) ? 1u : 0u;
   a.err = c.err;
   a.E = d.E;
   a.k = d.k;
   a.I = d.I;
   a.G = d.G;
-  a.gshift = d.G == 32 ? 5 : d.G == 64 ? 6 : 7;
   const int nC = c.fused_ctas;
   if (!plan_smem(c, nC, a.sm)) return cudaErrorInvalidConfiguration;
   ++*launches;

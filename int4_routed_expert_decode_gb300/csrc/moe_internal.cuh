@@ -13,6 +13,7 @@ constexpr int kMaxK = 32;
 constexpr int kMaxH = 8192;
 constexpr int kMaxInter = 4096;
 constexpr int kDecodeMaxT = 64;
+constexpr int kSyncWords = 1;  // counters of the fused decode kernel
 
 // Byte offsets of the four regions of one expert blob.  Layout of a blob
 // (all words uint32, offsets 256-byte aligned, 64-bit throughout):
@@ -44,8 +45,7 @@ struct Workspace {
   int32_t* hist;      // [nblk][E]   per-block expert counts (large T)
   float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
   float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
-  unsigned long long* bar;  // fused kernel: [0] CTAs done, [1] epoch of the tagged words
-  unsigned long long* tg;   // fused kernel: tagged words (value | epoch << 32)
+  unsigned long long* bar;  // fused kernel: grid-barrier arrival counter (monotonic)
 };
 
 struct Ctx {
@@ -103,8 +103,6 @@ cudaError_t prepare_general_experts(const Ctx& c);
 
 // Fused single-launch decode (T = 1): availability, one-time set-up, launch.
 bool fused_decode_supported(const Ctx& c);
-int tagged_h_index(int E);
-int64_t tagged_words(const Dims& d);
 cudaError_t prepare_fused_decode(Ctx& c);
 cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 

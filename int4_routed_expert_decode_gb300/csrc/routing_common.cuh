@@ -225,6 +225,55 @@ __device__ __forceinline__ void sort_lane_desc(uint32_t (&key)[N], int (&id)[N])
   }
 }
 
+// Bitonic sort across a warp of N = 32 V (key, id) pairs, best first (larger
+// key, then lower id; key 0 = empty sorts last).  Entry i = lane * V + v.
+// Stages with distance >= V exchange through shuffles, shorter ones stay in
+// registers (Batcher's bitonic network).
+template <int V>
+__device__ __forceinline__ void warp_bitonic_sort(uint32_t (&key)[V], int (&id)[V]) {
+  const int lane = threadIdx.x & 31;
+  constexpr int N = 32 * V;
+#pragma unroll
+  for (int kk = 2; kk <= N; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      if (j >= V) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int i = lane * V + v;
+          const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[v], j / V);
+          const int pid = __shfl_xor_sync(0xffffffffu, id[v], j / V);
+          const bool p_better = pk > key[v] || (pk == key[v] && pid < id[v]);
+          const bool lower = (i & j) == 0, up = (i & kk) == 0;
+          // in an "up" block the lower index keeps the better entry
+          if ((lower == up) ? p_better : !p_better && (pk != key[v] || pid != id[v])) {
+            key[v] = pk;
+            id[v] = pid;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int p = v ^ j;
+          if (p > v) {
+            const int i = lane * V + v;
+            const bool up = (i & kk) == 0;
+            const bool p_better = key[p] > key[v] || (key[p] == key[v] && id[p] < id[v]);
+            if (up ? p_better : !p_better) {
+              const uint32_t tk = key[v];
+              key[v] = key[p];
+              key[p] = tk;
+              const int ti = id[v];
+              id[v] = id[p];
+              id[p] = ti;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 // Swap entries p and q of the selection (and of the exact-value cache when
 // `cache` is given); one warp, positions relative to `base`.
 static __device__ __forceinline__ void swap_sel(int* sel_idx, float* sel_val, uint32_t* cache,

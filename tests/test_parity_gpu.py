@@ -335,8 +335,8 @@ def test_fused_decode_missing_slot_reported():
 
 
 def test_fused_decode_bounded_wait_reports_timeout():
-    """Waits for data stamped with an epoch nobody writes run out (about a
-    second each); the status says so and the context keeps working."""
+    """A grid barrier that waits for one CTA too many runs out (about a second);
+    the status says so and the context keeps working."""
     W = _weights(W0)
     L = U.layer(W0.shape, W, max_T=1)
     x = _x(W0, 1)
@@ -384,3 +384,18 @@ def test_fused_decode_graph_replay_of_stacked_layers():
         ref = O.moe_block(_x(wl, 1, layer=l, step=7), Ws[l], wl.k, wl.G)
         assert idx[l].cpu().numpy().tolist() == ref["topk_idx"].tolist()
         U.assert_y_close(U.to_f64_bf16(ys[l]), ref["y"], what=f"graph layer {l}")
+
+
+def test_fused_decode_topk_fallback_on_long_tie_chain():
+    """512 identical router rows: every logit ties; the exact comparison of a
+    run longer than the cached one settles the order (lowest ids first)."""
+    wl = synth.WORKLOADS[2]
+    W = _weights(wl, layer=9)
+    W["router_w"] = np.repeat(W["router_w"][:1], wl.E, axis=0)
+    L = U.layer(wl.shape, W, max_T=1)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+    x = _x(wl, 1, layer=9)
+    out = U.run(L, x)
+    assert out["topk_idx"].tolist() == [list(range(wl.k))]
+    ref = O.moe_block(x, W, wl.k, wl.G)
+    U.assert_parity(out, ref, what="tie chain")
