@@ -149,18 +149,25 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
 
 /* Kernel path of moe_forward.  MOE_PATH_AUTO uses the fused single-launch
  * decode kernel for T = 1 when the sizes allow it (hidden in {256, 512,
- * 1024, 2048}, inter == shared_inter <= 1024) and the general kernels
- * otherwise; MOE_PATH_DECODE insists on the fused kernel (MOE_ERR_UNSUPPORTED
- * if it cannot run); MOE_PATH_GENERAL forces the general kernels. */
+ * 1024, 2048}, inter == shared_inter <= 1024), the tensor-core grouped GEMMs
+ * for T > 64 when hidden, 2*inter and 2*shared_inter are multiples of 128,
+ * and the general kernels otherwise.  MOE_PATH_DECODE insists on the fused
+ * kernel and MOE_PATH_PREFILL on the grouped GEMMs (any T >= 1); either
+ * returns MOE_ERR_UNSUPPORTED if its sizes do not allow it.
+ * MOE_PATH_GENERAL forces the general kernels.  The grouped GEMMs round the
+ * dequantised weights and the SwiGLU activations to bf16 (tensor-core
+ * operands) and sum the expert outputs with fp32 atomic additions, so their
+ * y is not bitwise reproducible from run to run; the routing outputs are. */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_GENERAL = 2, MOE_PATH_PREFILL = 3 };
 int moe_set_path(moe_ctx* ctx, int path);
 
 /* Test hooks, off by default.  MOE_TEST_WAIT_TIMEOUT makes the grid
  * barriers of the fused decode kernel wait for one arrival more than the
- * grid has: each bounded wait runs out (about one second), the device
- * records MOE_ERR_TIMEOUT, and moe_get_status reports it and resets the
- * barrier counter so that the context stays usable.  flags = 0 turns every
- * hook off. */
+ * grid has, and the MMA issuer of each grouped-GEMM CTA wait on an mbarrier
+ * phase that nothing completes: each bounded wait runs out (about one
+ * second), the device records MOE_ERR_TIMEOUT, every role of the CTA leaves
+ * its loop, and moe_get_status reports it and resets the barrier counter so
+ * that the context stays usable.  flags = 0 turns every hook off. */
 enum { MOE_TEST_WAIT_TIMEOUT = 1 };
 int moe_set_test_flags(moe_ctx* ctx, int flags);
 

@@ -289,6 +289,8 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_o = take(rows * d.H * 4);
   const uint64_t o_err = take(4);
   const uint64_t o_bar = take(kSyncWords * 8);
+  const uint64_t o_tiles = take((uint64_t)prefill_max_tiles(d, max_T) * 16);
+  const uint64_t o_ntiles = take(4);
   uint8_t* base = nullptr;
   cudaError_t e = cudaMalloc(&base, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace alloc");
@@ -313,9 +315,17 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.o = (float*)(base + o_o);
   c.err = (int32_t*)(base + o_err);
   c.ws.bar = (unsigned long long*)(base + o_bar);
+  c.ws.tiles = base + o_tiles;
+  c.ws.n_tiles = (int32_t*)(base + o_ntiles);
   c.max_T = max_T;
+  if ((e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, c.device)) !=
+      cudaSuccess) {
+    free_workspace(c);
+    return cuda_fail(ctx, e, "device attributes");
+  }
   if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess ||
-      (e = prepare_fused_decode(c)) != cudaSuccess) {
+      (e = prepare_fused_decode(c)) != cudaSuccess ||
+      (prefill_supported(d) && (e = prepare_prefill(c)) != cudaSuccess)) {
     free_workspace(c);
     return cuda_fail(ctx, e, "kernel attributes");
   }
@@ -348,9 +358,15 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   FwdArgs a{(const uint16_t*)x, T, expert_slot_table, (uint16_t*)y, topk_idx, topk_w, perm, offsets};
   int launches = 0;
   const bool fused_ok = T == 1 && fused_decode_supported(c);
+  const bool prefill_ok = prefill_supported(c.d);
   if (c.path == MOE_PATH_DECODE && !fused_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
                    "the fused decode path needs T = 1 and supported sizes");
+  if (c.path == MOE_PATH_PREFILL && !prefill_ok)
+    return set_msg(ctx, MOE_ERR_UNSUPPORTED,
+                   "the prefill path needs hidden and 2*inter multiples of 128");
+  const bool use_prefill =
+      c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > kDecodeMaxT);
   cudaError_t e;
   if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE)) {
     e = launch_fused_decode(c, a, st, &launches);
@@ -358,7 +374,9 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
     e = launch_router(c, a, st, &launches);
     if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
     if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
-    if (e == cudaSuccess) e = launch_general_experts(c, a, st, &launches);
+    if (e == cudaSuccess)
+      e = use_prefill ? launch_prefill_experts(c, a, st, &launches)
+                      : launch_general_experts(c, a, st, &launches);
   }
   c.last_launches = launches;
   if (e != cudaSuccess) return cuda_fail(ctx, e, "moe_forward launch");

@@ -46,6 +46,8 @@ struct Workspace {
   float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
   float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
   unsigned long long* bar;  // fused kernel: grid-barrier arrival counter (monotonic)
+  void* tiles;        // [max tiles] prefill work tiles (16 bytes each)
+  int32_t* n_tiles;   // [1]
 };
 
 struct Ctx {
@@ -68,6 +70,7 @@ struct Ctx {
   int64_t ws_bytes = 0;
   Workspace ws{};
   int32_t* err = nullptr;             // sticky device error word
+  int num_sms = 0;                    // multiprocessors of the device
   int fused_ctas = 0;                 // CTAs of the fused decode kernel (0: unavailable)
   int test_flags = 0;                 // MOE_TEST_* hooks
   int last_launches = 0;
@@ -105,6 +108,15 @@ cudaError_t prepare_general_experts(const Ctx& c);
 bool fused_decode_supported(const Ctx& c);
 cudaError_t prepare_fused_decode(Ctx& c);
 cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+
+// Tensor-core grouped GEMM path for many tokens: availability, workspace
+// size (tiles for max_T tokens), one-time set-up, launch (after router, top-k
+// and permutation).
+bool prefill_supported(const Dims& d);
+int prefill_max_tiles(const Dims& d, int max_T);
+cudaError_t prepare_prefill(const Ctx& c);
+cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
+                                   int* launches);
 
 cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);

@@ -399,3 +399,136 @@ def test_fused_decode_topk_fallback_on_long_tie_chain():
     assert out["topk_idx"].tolist() == [list(range(wl.k))]
     ref = O.moe_block(x, W, wl.k, wl.G)
     U.assert_parity(out, ref, what="tie chain")
+
+
+# ------------------------------------------------------------------ tensor-core grouped GEMMs
+def _prefill_layer(shape, W, max_T, **kw):
+    L = U.layer(shape, W, max_T=max_T, **kw)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_PREFILL)
+    return L
+
+
+@pytest.mark.parametrize("T", [1, 4, 17, 130, 300])
+def test_prefill_path_tiny_ragged(T):
+    """One to three 128-token tiles per expert, ragged tails, N from 16 up."""
+    W = _weights(W0, layer=3)
+    x = _x(W0, T, layer=3, step=T)
+    L = _prefill_layer(W0.shape, W, max_T=300)
+    ref = O.moe_block(x, W, W0.k, W0.G)
+    U.assert_parity(U.run(L, x), ref, what=f"prefill T={T}")
+
+
+def test_prefill_path_hot_experts_span_many_tiles():
+    """Zipf-skewed routing: hot experts own several full tiles; I != Is."""
+    shape = synth.Shape(E=16, k=5, H=256, I=64, Is=128, G=32)
+    W = synth.layer_weights(0, 0, 7, shape, zipf_s=1.1)
+    x = synth.tokens(0, 0, 7, 1, 700, shape.H)
+    L = _prefill_layer(shape, W, max_T=700)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    assert np.diff(ref["offsets"]).max() > 3 * 128
+    U.assert_parity(U.run(L, x), ref, what="prefill zipf")
+
+
+def test_prefill_path_group_128_wide_hidden():
+    shape = synth.Shape(E=32, k=4, H=1024, I=256, Is=128, G=128)
+    W = synth.layer_weights(0, 0, 9, shape)
+    x = synth.tokens(0, 0, 9, 2, 200, shape.H)
+    L = _prefill_layer(shape, W, max_T=200)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="prefill G=128")
+
+
+def test_prefill_path_full_width_expert_shapes():
+    """hidden 2048, inter 512, group 64 (the 35B/80B expert shapes), fewer experts."""
+    shape = synth.Shape(E=64, k=8, H=2048, I=512, Is=512, G=64)
+    W = synth.layer_weights(0, 0, 11, shape, zipf_s=0.8)
+    x = synth.tokens(0, 0, 11, 0, 160, shape.H)
+    L = _prefill_layer(shape, W, max_T=160)
+    ref = O.moe_block(x, W, shape.k, shape.G)
+    U.assert_parity(U.run(L, x), ref, what="prefill 2048x512")
+
+
+def test_prefill_path_batched_decode_workload():
+    """The 64-token Zipf(1.1) batch through the grouped GEMMs, every row checked."""
+    wl = synth.WORKLOADS[3]
+    W = _weights(wl)
+    x = _x(wl, wl.T)
+    L = _prefill_layer(wl.shape, W, max_T=wl.T)
+    ref = O.moe_block(x, W, wl.k, wl.G)
+    U.assert_parity(U.run(L, x), ref, what="batch64 prefill path")
+
+
+def test_prefill_path_agrees_with_general_path():
+    W = _weights(W0, layer=4)
+    x = _x(W0, 257, layer=4)
+    Lp = _prefill_layer(W0.shape, W, max_T=257)
+    Lg = U.layer(W0.shape, W, max_T=257)
+    moe.moe_set_path(Lg.ctx, moe.MOE_PATH_GENERAL)
+    a, b = U.run(Lp, x), U.run(Lg, x)
+    assert np.array_equal(a["topk_idx"], b["topk_idx"])
+    assert np.array_equal(a["perm"], b["perm"])
+    U.assert_y_close(a["y"], b["y"], what="prefill vs general")
+
+
+def test_general_path_many_tokens():
+    W = _weights(W0, layer=5)
+    x = _x(W0, 200, layer=5)
+    L = U.layer(W0.shape, W, max_T=200)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_GENERAL)
+    U.assert_parity(U.run(L, x), O.moe_block(x, W, W0.k, W0.G), what="general T=200")
+
+
+def test_prefill_path_missing_slot_reported():
+    W = _weights(W0)
+    x = _x(W0, 100)
+    L = _prefill_layer(W0.shape, W, max_T=100)
+    table = np.arange(W0.E, dtype=np.int32)
+    table[3] = -1
+    out = U.run(L, x, table=table)
+    assert out["status"] == moe.MOE_ERR_SLOT
+    out = U.run(L, x)
+    U.assert_parity(out, O.moe_block(x, W, W0.k, W0.G), what="after slot error")
+
+
+def test_prefill_path_bounded_wait_reports_timeout():
+    """The MMA issuer of each CTA waits on a phase nothing completes: the wait
+    runs out, every role of the CTA leaves, the status says so, and the
+    context keeps working."""
+    W = _weights(W0)
+    x = _x(W0, 100)
+    L = _prefill_layer(W0.shape, W, max_T=100)
+    moe.moe_set_test_flags(L.ctx, moe.MOE_TEST_WAIT_TIMEOUT)
+    out = U.run(L, x)
+    assert out["status"] == moe.MOE_ERR_TIMEOUT
+    moe.moe_set_test_flags(L.ctx, 0)
+    out = U.run(L, x)
+    U.assert_parity(out, O.moe_block(x, W, W0.k, W0.G), what="after timeout")
+
+
+def test_prefill_path_graph_replay():
+    """The whole prefill sequence (router to y) captured in a CUDA graph
+    matches the oracle on every replay."""
+    import torch
+    W = _weights(W0, layer=6)
+    T = 150
+    x_np = _x(W0, T, layer=6)
+    L = _prefill_layer(W0.shape, W, max_T=T)
+    x = torch.from_numpy(x_np.view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((T, W0.H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, W0.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, W0.k), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe.moe_forward(L.ctx, x, T, None, y, idx, w, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_forward(L.ctx, x, T, None, y, idx, w, stream=s)
+    ref = O.moe_block(x_np, W, W0.k, W0.G)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert L.status() == moe.MOE_OK
+        assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
+        U.assert_y_close(U.to_f64_bf16(y), ref["y"], what="prefill graph")
