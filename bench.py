@@ -211,6 +211,37 @@ def config_of(wl, L, note=None):
 
 
 # --------------------------------------------------------------------- our arm
+STAGES = ("router", "topk", "permute", "gateup", "down", "combine")
+
+
+def stage_times(moe, torch, ctx, enqueue, inputs, stream, k):
+    """Mean device time of each stage of the first layer's moe_forward over k
+    eager steps, from the library's stage events (recorded on the launching
+    stream).  Stages a path does not have are absent."""
+    sets = []
+    with torch.cuda.stream(stream):
+        for i in range(k):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_MARK_COUNT)]
+            for e in evs:
+                e.record(stream)  # creates the event; a later record by the library moves it
+            sets.append(evs)
+        stream.synchronize()
+        for i in range(k):
+            moe.moe_set_stage_events(ctx, sets[i])
+            enqueue(inputs[i % len(inputs)])
+        moe.moe_set_stage_events(ctx, [])
+        stream.synchronize()
+    acc = {}
+    for evs in sets:
+        marks = [0.0] + [evs[0].elapsed_time(evs[m]) for m in range(1, moe.MOE_MARK_COUNT)]
+        seen = [m for m in range(moe.MOE_MARK_COUNT) if m == 0 or marks[m] >= 0.0]
+        for a, b in zip(seen, seen[1:]):
+            name = STAGES[a] if b == a + 1 else "+".join(STAGES[a:b])
+            acc.setdefault(name, []).append((marks[b] - marks[a]) * 1e3)
+        acc.setdefault("total", []).append(marks[moe.MOE_MARK_END] * 1e3)
+    return {n: float(np.mean(v)) for n, v in acc.items()}
+
+
 def run_ours(args, wl):
     import torch
 
@@ -307,6 +338,9 @@ def run_ours(args, wl):
             torch.distributed.barrier()
         ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
+    # per-stage device times of layer 0 (eager, same stream, after the timed region)
+    stages = stage_times(moe, torch, layers[0].ctx, enqueue, [x_all[s] for s in range(S)],
+                         stream, k=max(3, min(args.steps, 20)))
     t_max = ms
     if world > 1:
         tt = torch.tensor([ms], device="cuda")
@@ -358,22 +392,40 @@ def run_ours(args, wl):
         if errs:
             parity = {"checked_passes": len(errs), "max_rel_err": max(errs)}
 
-    algo_bytes_layer = unique_per_step / L + wl.router_bytes + 2 * T * H * 2
-    achieved = algo_bytes_layer / (us_layer * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None,
-                "kernel": f"one layer of moe_forward ({launches_per_layer} launches), "
-                          f"{algo_bytes_layer / 1e6:.2f} MB algorithmic per layer",
-                "peak_source": pk["source"]}
+    P = T * wl.k
+    flops = {"gateup": 2.0 * H * (2 * wl.I * P + 2 * wl.Is * T),
+             "down": 2.0 * H * (wl.I * P + wl.Is * T), "router": 2.0 * H * wl.E * T}
+    flops_layer = sum(flops.values())
+    grouped = args.path == 3 or (args.path == 0 and T > 64)  # tensor-core grouped GEMMs
+    if grouped:
+        # many tokens: the grouped GEMMs are tensor-core bound; the gate/up GEMM dominates
+        t_gu = stages["gateup"] * 1e-6
+        achieved = flops["gateup"] / t_gu / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                    "kernel": "grouped_gemm_kernel<gate/up> (tcgen05 bf16, fp32 TMEM), "
+                              f"{flops['gateup'] / 1e9:.1f} GFLOP algorithmic per launch, "
+                              f"{stages['gateup']:.1f} us per launch",
+                    "peak_source": pk["source"] + " burst bf16 (cuBLAS)"}
+    else:
+        algo_bytes_layer = unique_per_step / L + wl.router_bytes + 2 * T * H * 2
+        achieved = algo_bytes_layer / (us_layer * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                    "kernel": f"one layer of moe_forward ({launches_per_layer} launches), "
+                              f"{algo_bytes_layer / 1e6:.2f} MB algorithmic per layer",
+                    "peak_source": pk["source"]}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if grouped else "fp32", "data": "synthetic",
         "config": config_of(wl, L, note="inputs larger than L2: each step touches "
                             f"{unique_per_step / 1e6:.0f} MB of distinct expert weights; "
                             f"{S} distinct step inputs rotate"),
         "us_per_layer": us_layer, "stack_tokens_per_s": world * T / (ms_step / 1e3),
         "hbm_gbs_unique_expert_bytes": hbm, "hbm_frac": hbm / pk["hbm_gbs"],
+        "tflops_layer": flops_layer / (us_layer * 1e-6) / 1e12,
+        "stages_us_layer0": stages,
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": L * T * H * 2,
                 "d2h_bytes_per_step": L * T * H * 2},

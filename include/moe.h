@@ -171,6 +171,34 @@ int moe_set_path(moe_ctx* ctx, int path);
 enum { MOE_TEST_WAIT_TIMEOUT = 1 };
 int moe_set_test_flags(moe_ctx* ctx, int flags);
 
+/* Optional device timing of moe_forward's stages.  `events` holds
+ * n_events (<= MOE_MARK_COUNT) cudaEvent_t handles that the caller created
+ * with timing enabled.  While they are set, moe_forward records events[m] on
+ * its stream at each mark m that its path has:
+ *   MOE_MARK_START     before the first launch (every path)
+ *   MOE_MARK_LOGITS    router logits written
+ *   MOE_MARK_ROUTED    top-k indices and weights written
+ *   MOE_MARK_PERMUTED  permutation (and the grouped GEMMs' tile list) done
+ *   MOE_MARK_GATEUP    gate/up projections and SwiGLU done
+ *   MOE_MARK_DOWN      down projections done
+ *   MOE_MARK_END       y written (every path)
+ * The fused decode kernel has START and END only.  The handles are borrowed
+ * until the next call; n_events = 0 turns the marks off.  Inside a stream
+ * capture the records become event-record nodes of the graph.
+ * MOE_ERR_INVALID_ARG if n_events is out of range or events is NULL with
+ * n_events > 0. */
+enum {
+  MOE_MARK_START = 0,
+  MOE_MARK_LOGITS = 1,
+  MOE_MARK_ROUTED = 2,
+  MOE_MARK_PERMUTED = 3,
+  MOE_MARK_GATEUP = 4,
+  MOE_MARK_DOWN = 5,
+  MOE_MARK_END = 6,
+  MOE_MARK_COUNT = 7
+};
+int moe_set_stage_events(moe_ctx* ctx, void* const* events, int n_events);
+
 /* Bytes of one routed-expert blob (codes + scales + biases, padded) and the
  * number of resident device bytes of the context (weights + workspace). */
 int64_t moe_expert_blob_bytes(const moe_ctx* ctx);

@@ -28,13 +28,15 @@ MOE_ERR_UNSUPPORTED = -8
 
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_GENERAL, MOE_PATH_PREFILL = 0, 1, 2, 3
 MOE_TEST_WAIT_TIMEOUT = 1
+(MOE_MARK_START, MOE_MARK_LOGITS, MOE_MARK_ROUTED, MOE_MARK_PERMUTED, MOE_MARK_GATEUP,
+ MOE_MARK_DOWN, MOE_MARK_END, MOE_MARK_COUNT) = range(8)
 
 # every symbol include/moe.h declares
 EXPORTS = (
     "moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
     "moe_read_expert", "moe_set_path", "moe_expert_blob_bytes", "moe_device_bytes",
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
-    "moe_route_static", "moe_set_test_flags",
+    "moe_route_static", "moe_set_test_flags", "moe_set_stage_events",
 )
 
 
@@ -80,6 +82,7 @@ def lib():
     L.moe_read_expert.argtypes = [vp, i32] + [vp] * 9
     L.moe_set_path.argtypes = [vp, i32]
     L.moe_set_test_flags.argtypes = [vp, i32]
+    L.moe_set_stage_events.argtypes = [vp, ctypes.POINTER(vp), i32]
     L.moe_expert_blob_bytes.argtypes = [vp]
     L.moe_expert_blob_bytes.restype = i64
     L.moe_device_bytes.argtypes = [vp]
@@ -95,7 +98,7 @@ def lib():
     L.moe_route_static.restype = i32
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
                  "moe_read_expert", "moe_set_path", "moe_last_launch_count",
-                 "moe_set_test_flags"):
+                 "moe_set_test_flags", "moe_set_stage_events"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -214,6 +217,15 @@ def moe_set_path(ctx: int, path: int):
 
 def moe_set_test_flags(ctx: int, flags: int):
     _check(lib().moe_set_test_flags(ctx, flags), ctx)
+
+
+def moe_set_stage_events(ctx: int, events):
+    """Borrow cudaEvent_t handles (ints, or torch.cuda.Event objects that have
+    been recorded once, so that they exist) for the stage marks; [] turns
+    the marks off."""
+    hs = [e if isinstance(e, int) else int(e.cuda_event) for e in events]
+    arr = (ctypes.c_void_p * max(1, len(hs)))(*hs)
+    _check(lib().moe_set_stage_events(ctx, arr if hs else None, len(hs)), ctx)
 
 
 def moe_expert_blob_bytes(ctx: int) -> int:

@@ -279,6 +279,12 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_bound = take((uint64_t)max_T * d.E * 4);
   const uint64_t o_gz = take((uint64_t)max_T * 4);
   const uint64_t o_gate = take((uint64_t)max_T * 4);
+  const uint64_t o_xnorm = take((uint64_t)max_T * 4);
+  const uint64_t o_wnorm = take((uint64_t)d.E * 4);
+  int n_sms = 0;
+  if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess)
+    n_sms = 160;
+  const uint64_t o_rpart = take((uint64_t)tile_router_part_floats(n_sms) * 4);
   const uint64_t o_perm = take(P * 4);
   const uint64_t o_inv = take(P * 4);
   const uint64_t o_off = take((uint64_t)(d.E + 1) * 4);
@@ -305,6 +311,9 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.bound = (float*)(base + o_bound);
   c.ws.gate_z = (float*)(base + o_gz);
   c.ws.gate = (float*)(base + o_gate);
+  c.ws.xnorm = (float*)(base + o_xnorm);
+  c.ws.wnorm = (float*)(base + o_wnorm);
+  c.ws.rpart = (float*)(base + o_rpart);
   c.ws.perm = (int32_t*)(base + o_perm);
   c.ws.inv = (int32_t*)(base + o_inv);
   c.ws.offsets = (int32_t*)(base + o_off);
@@ -368,16 +377,22 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   const bool use_prefill =
       c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > kDecodeMaxT);
   cudaError_t e;
+  record_mark(c, MOE_MARK_START, st);
   if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE)) {
     e = launch_fused_decode(c, a, st, &launches);
   } else {
     e = launch_router(c, a, st, &launches);
+    record_mark(c, MOE_MARK_LOGITS, st);
     if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+    record_mark(c, MOE_MARK_ROUTED, st);
     if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
+    if (e == cudaSuccess && use_prefill) e = launch_prefill_plan(c, a, st, &launches);
+    record_mark(c, MOE_MARK_PERMUTED, st);
     if (e == cudaSuccess)
       e = use_prefill ? launch_prefill_experts(c, a, st, &launches)
                       : launch_general_experts(c, a, st, &launches);
   }
+  record_mark(c, MOE_MARK_END, st);
   c.last_launches = launches;
   if (e != cudaSuccess) return cuda_fail(ctx, e, "moe_forward launch");
   return MOE_OK;
@@ -462,6 +477,18 @@ int moe_set_test_flags(moe_ctx* ctx, int flags) {
   if (flags & ~MOE_TEST_WAIT_TIMEOUT)
     return set_msg(ctx, MOE_ERR_INVALID_ARG, "unknown test flag %d", flags);
   ctx->c.test_flags = flags;
+  return MOE_OK;
+}
+
+int moe_set_stage_events(moe_ctx* ctx, void* const* events, int n_events) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (n_events < 0 || n_events > MOE_MARK_COUNT || (n_events > 0 && !events))
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "n_events=%d not in [0, %d] or events NULL",
+                   n_events, (int)MOE_MARK_COUNT);
+  Ctx& c = ctx->c;
+  for (int i = 0; i < MOE_MARK_COUNT; ++i)
+    c.marks[i] = i < n_events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  c.n_marks = n_events;
   return MOE_OK;
 }
 

@@ -243,6 +243,7 @@ cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t 
         a.x, T, d.k, d.H, d.I, d.Is, d.G, c.ws.perm, c.ws.offsets, c.ws.used, c.ws.n_used,
         a.table, c.n_slots, c.pool, c.ex, c.shared, c.sh, maxI, c.ws.h, tc, c.err);
     ++*launches;
+    record_mark(c, MOE_MARK_GATEUP, st);
   }
   {
     const int tc = pick_tc(maxI);
@@ -252,6 +253,7 @@ cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t 
         T, d.k, d.H, d.I, d.Is, d.G, c.ws.offsets, c.ws.used, c.ws.n_used, a.table, c.n_slots,
         c.pool, c.ex, c.shared, c.sh, maxI, c.ws.h, c.ws.o, tc, c.err);
     ++*launches;
+    record_mark(c, MOE_MARK_DOWN, st);
   }
   combine_kernel<<<T, 256, 0, st>>>(T, d.k, d.H, a.topk_w, c.ws.inv, c.ws.gate, c.ws.o, a.y);
   ++*launches;

@@ -14,6 +14,10 @@ constexpr int kMaxH = 8192;
 constexpr int kMaxInter = 4096;
 constexpr int kDecodeMaxT = 64;
 constexpr int kSyncWords = 1;  // counters of the fused decode kernel
+constexpr int kTileRouterMinT = 16;  // from this many tokens the router is a tiled GEMM
+// Floats of the router's slice sums: the slices are only used while
+// slices x tiles <= 2 x SMs, and a tile covers 64 x 128 logits.
+inline int64_t tile_router_part_floats(int num_sms) { return (int64_t)2 * num_sms * 64 * 128; }
 
 // Byte offsets of the four regions of one expert blob.  Layout of a blob
 // (all words uint32, offsets 256-byte aligned, 64-bit throughout):
@@ -37,6 +41,9 @@ struct Workspace {
   float* bound;       // [max_T][E]  rigorous bound on their rounding error
   float* gate_z;      // [max_T]     x . wsg (shared gate pre-activation)
   float* gate;        // [max_T]     sigmoid(x . wsg)
+  float* xnorm;       // [max_T]     upper bound of |x_t|_2 (many-token router)
+  float* wnorm;       // [E]         upper bound of |Wr_e|_2
+  float* rpart;       // many-token router: slice sums [slices][T][E]
   int32_t* perm;      // [max_T*k]   pair ids sorted by expert
   int32_t* inv;       // [max_T*k]   position of pair p in perm
   int32_t* offsets;   // [E+1]
@@ -73,6 +80,8 @@ struct Ctx {
   int num_sms = 0;                    // multiprocessors of the device
   int fused_ctas = 0;                 // CTAs of the fused decode kernel (0: unavailable)
   int test_flags = 0;                 // MOE_TEST_* hooks
+  cudaEvent_t marks[MOE_MARK_COUNT] = {};  // borrowed stage events (moe_set_stage_events)
+  int n_marks = 0;
   int last_launches = 0;
   char msg[512] = {0};
 };
@@ -115,6 +124,7 @@ cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st,
 bool prefill_supported(const Dims& d);
 int prefill_max_tiles(const Dims& d, int max_T);
 cudaError_t prepare_prefill(const Ctx& c);
+cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
 
@@ -123,6 +133,11 @@ cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* la
 cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
+
+// Record stage event `m` on `st` if the caller set one (moe_set_stage_events).
+inline void record_mark(const Ctx& c, int m, cudaStream_t st) {
+  if (m < c.n_marks && c.marks[m]) cudaEventRecord(c.marks[m], st);
+}
 
 // Set the message returned by moe_last_error(NULL); returns `code`.
 int set_global_msg(int code, const char* text);

@@ -16,23 +16,38 @@
 //             w_tj * D into an fp32 [T][hidden] accumulator (reductions in
 //             L2); the shared expert's weight is sigmoid(x . wsg).
 //
+// Operand paths.  The token rows (B) arrive by per-thread asynchronous copies
+// (any row ids; eight lanes per 128-byte row segment, so a warp moves four
+// whole rows per instruction) straight into the 128-byte-swizzled K-major
+// layout the tensor core reads from shared memory.  The packed int4 codes
+// arrive by 3-D TMA tile copies, the scale/bias words of up to 32 groups per
+// row at a time into a double-buffered window, and the weights (A) are
+// dequantised (MLX affine, w = s q + b; Swiftlet README,
+// "MLX affine int4/int8 group quantization") to bf16 straight into tensor
+// memory, which the MMA reads as its A operand: A costs no shared-memory
+// bandwidth and no proxy fence.
+//
 // The kernel is persistent (one CTA per SM walks the units in a fixed
-// stride) and warp-specialised:
-//   warp 0      issues tcgen05.mma (one thread) into one of two TMEM
-//               accumulators, so the epilogue of a unit overlaps the next
-//               unit's main loop;
-//   warps 1-7   produce K-chunks of 64: per-thread asynchronous copies bring
-//               the packed int4 codes, the scale/bias words and the token rows
-//               (the latter straight into the 128-byte-swizzled K-major layout
-//               the tensor core reads); the codes are then dequantised (MLX
-//               affine, w = s q + b; Swiftlet README, "MLX affine int4/int8
-//               group quantization") to bf16 into the same layout;
-//   warps 8-11  epilogue: tcgen05.ld of the accumulator, SwiGLU or the
-//               weighted reduction.
-// A ring of 4 shared-memory stages with full/empty mbarriers connects
-// producers and MMA; the copies run two chunks ahead of the dequantisation.
+// stride) and warp-specialised, so that no warp both waits for memory and
+// computes:
+//   warp 0       issues tcgen05.mma (one thread) into one of two TMEM
+//                accumulators, so the epilogue of a unit overlaps the next
+//                unit's main loop;
+//   warps 1-8    loaders: for each K-chunk of 64, once its stage is free, the
+//                copies (a ring of 8 stages; eight warps, because one warp's
+//                gathers cannot keep up); each lane marks a stage full
+//                kAhead chunks later, once its own copies have landed and are
+//                fenced for the tensor core (the TMA copy of the codes counts
+//                on the same mbarrier);
+//   warps 9-16   dequantise a landed stage into the stage's TMEM A tile (two
+//                warps per TMEM lane quarter, one K-half each);
+//   warps 17-20  epilogue: tcgen05.ld of the accumulator, then SwiGLU (gate/
+//                up) or the routing-weighted fp32 vector reductions (down),
+//                both through a small shared-memory transpose so that every
+//                global access is 16 bytes wide.
 // Every wait is bounded (1 s): on expiry the kernel records MOE_ERR_TIMEOUT,
 // all roles leave their loops and the TMEM is released.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "device_util.cuh"
@@ -46,22 +61,28 @@ namespace {
 constexpr int kBM = 128;       // weight rows per unit (UMMA M)
 constexpr int kBN = 128;       // tokens per tile (largest UMMA N used)
 constexpr int kBK = 64;        // K per chunk: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
-constexpr int kAhead = 2;      // chunks whose copies are in flight ahead of the dequantisation
-constexpr int kProdWarps = 7;
-constexpr int kProdThreads = kProdWarps * 32;
-constexpr int kEpiWarp0 = 1 + kProdWarps;       // 8: TMEM lane quarter = warp % 4
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;  // 384
-constexpr int kAccCols = 128;  // TMEM columns per accumulator
-constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kTileBytes = kBM * kBK * 2;  // 16 KiB (A and B alike)
-constexpr int kRawCodes = kBM * kBK / 2;   // 4 KiB of packed codes per chunk
-constexpr int kRawSbWords = kBM * 2;       // up to 2 scale/bias words per row per chunk
+constexpr int kStages = 8;     // token rows + packed codes + scale/bias words, and a TMEM A tile
+constexpr int kAhead = 3;      // chunks of copies in flight before the loader marks one full
+constexpr int kDqWarps = 8;
+constexpr int kLoadWarps = 8;
+constexpr int kLoad0 = 1, kDq0 = kLoad0 + kLoadWarps, kEpi0 = kDq0 + kDqWarps;  // warp roles
+constexpr int kThreads = (kEpi0 + 4) * 32;  // 672
+constexpr int kAccCols = 128;               // TMEM columns per accumulator
+constexpr int kACols = kBK / 2;             // TMEM columns per A stage (2 bf16 per column)
+constexpr int kACol0 = 2 * kAccCols;        // first A column
+constexpr int kTmemCols = 512;
+constexpr int kTileBytes = kBN * kBK * 2;   // 16 KiB of token rows
+constexpr int kCodesOff = kTileBytes;       // in a raw stage: 4 KiB of codes
+constexpr int kCodesBytes = kBM * 32;
+constexpr int kRawStride = kTileBytes + kCodesBytes;  // 20 KiB, 1 KiB aligned
+constexpr int kSbWin = 32;                  // scale/bias words per row in a window
+constexpr int kEpiStride = 36;              // floats per transposed column (bank spread)
 constexpr uint64_t kWaitNs = 1000000000ull;
-constexpr int kBarProd = 1, kBarEpi = 2;   // named barrier ids
+constexpr int kBarEpi = 1;                  // named barrier of the epilogue warps
 
-static_assert(kStages >= kAhead + 2, "the stage a copy targets must be two MMAs old");
-static_assert(kBN == kBM, "one producer thread per token row of B");
+static_assert(kDqWarps == 8, "two dequantising warps per TMEM lane quarter");
+static_assert(kACol0 + kStages * kACols <= kTmemCols, "TMEM budget");
+static_assert(kAhead < kStages, "the loader must mark a stage full before it needs that stage again");
 
 struct Tile {
   int slot;   // expert slot, or -1 for the shared expert
@@ -89,11 +110,11 @@ struct GemmArgs {
 };
 
 struct Smem {
-  uint8_t a[kStages][kTileBytes];  // dequantised weights, swizzled K-major
-  uint8_t b[kStages][kTileBytes];  // token rows, swizzled K-major
-  uint8_t raw[kStages][kRawCodes];
-  uint32_t rsb[kStages][kRawSbWords];
-  uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
+  uint8_t raw[kStages][kRawStride];  // token rows (swizzled), codes
+  uint32_t sb[2][kBM * kSbWin];      // scale/bias windows [row][word]
+  float epi[4][16 * kEpiStride];     // per epilogue warp: 16 columns x 32 rows
+  uint64_t raw_full[kStages], a_full[kStages], empty[kStages], sb_full[2], sb_empty[2];
+  uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
   int abort;
   int tok_t[kBN];
@@ -118,17 +139,19 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
-// Byte offset of 16-byte chunk `ch` (0..7) of row `row` in a swizzled tile.
+// Byte offset of 16-byte chunk `ch` (0..7) of row `row` in a swizzled tile
+// (the tile 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
   return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4));
 }
 
 // ---- dequantisation --------------------------------------------------------
 // 32 codes (one uint4; code 8j+i at bits 4i of word j) with their group's
-// scale s and bias b -> 32 bf16 in four 16-byte chunks.  In fp32,
-// 1 + q/128 is built by byte permutation, and s q + b = (128 s)(1 + q/128) +
-// (b - 128 s): one FMA per code, then round to nearest even bf16.
-__device__ __forceinline__ void dequant32(uint4 w, uint32_t sb, uint4 (&out)[4]) {
+// scale s and bias b -> 32 bf16, two per 32-bit word (lower k in the low
+// half).  In fp32, 1 + q/128 is built by byte permutation, and
+// s q + b = (128 s)(1 + q/128) + (b - 128 s): one FMA per code, then round to
+// nearest even bf16.
+__device__ __forceinline__ void dequant32(uint4 w, uint32_t sb, uint32_t (&out)[16]) {
   const float s128 = 128.0f * bf16_lo(sb);
   const float off = bf16_hi(sb) - s128;
   const float2 s2 = make_float2(s128, s128), o2 = make_float2(off, off);
@@ -137,16 +160,14 @@ __device__ __forceinline__ void dequant32(uint4 w, uint32_t sb, uint4 (&out)[4])
   for (int j = 0; j < 4; ++j) {
     const uint32_t lo = (ws[j] & 0x0F0F0F0Fu) | 0x80808080u;         // codes 0, 2, 4, 6
     const uint32_t hi = ((ws[j] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;  // codes 1, 3, 5, 7
-    uint32_t pk[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float f0 = __uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044u | (b << 8)));
       const float f1 = __uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044u | (b << 8)));
       const float2 v = __ffma2_rn(s2, make_float2(f0, f1), o2);
       const __nv_bfloat162 p = __floats2bfloat162_rn(v.x, v.y);
-      pk[b] = *reinterpret_cast<const uint32_t*>(&p);
+      out[4 * j + b] = *reinterpret_cast<const uint32_t*>(&p);
     }
-    out[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
@@ -215,8 +236,12 @@ struct Walk {
   }
 };
 
+// cmap / cmap_sh: the packed codes of the routed pool / the shared blob,
+// 3-D uint32 {K/8, rows, blobs}, box 8 x 128 x 1.
 template <bool DOWN>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap cmap,
+                        const __grid_constant__ CUtensorMap cmap_sh) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,8 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&S.full[s], kProdWarps);
+      ptx::mbar_init(&S.raw_full[s], kLoadWarps * 32 + 1);  // loader lanes + the expect-tx arrival
+      ptx::mbar_init(&S.a_full[s], kDqWarps);
       ptx::mbar_init(&S.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&S.sb_full[b], kLoadWarps * 32);  // one copy arrival per loader lane
+      ptx::mbar_init(&S.sb_empty[b], kDqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&S.acc_full[b], 1);
@@ -240,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  // scale/bias windows: up to kSbWin group words per row, i.e. cpw chunks
+  const int cpw = kSbWin * a.G / kBK;
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
@@ -259,16 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
         const uint32_t d = tmem + buf * kAccCols;
         do {
           const int s = g % kStages;
-          if (!wait_phase(&S.full[s], (g / kStages) & 1, S, a.err)) {
+          const uint32_t par = (g / kStages) & 1;
+          if (!wait_phase(&S.a_full[s], par, S, a.err) || !wait_phase(&S.raw_full[s], par, S, a.err)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(S.a[s]), sbb = ptx::smem_u32(S.b[s]);
+          const uint32_t at = tmem + kACol0 + s * kACols;
+          const uint32_t bb = ptx::smem_u32(S.raw[s]);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            ptx::tc_mma_f16(d, sw128_desc(sa + kk * 32), sw128_desc(sbb + kk * 32), idesc,
-                            (w.c > 0 || kk > 0) ? 1u : 0u);
+            ptx::tc_mma_f16_ta(d, at + kk * 8, sw128_desc(bb + kk * 32), idesc,
+                               (w.c > 0 || kk > 0) ? 1u : 0u);
           ptx::tc_commit(&S.empty[s]);
           ++g;
         } while (!w.next(a));
@@ -281,116 +315,138 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
       wait_phase(&S.drain, 0, S, a.err);
     }
     __syncwarp();
-  } else if (warp < kEpiWarp0) {
-    // ------------------------------------------------------------ producers
-    const int pt = threadIdx.x - 32;  // 0 .. 223
-    const int sbw = a.G < kBK ? kBK / a.G : 1;  // scale/bias words per row per chunk
-    Walk<DOWN> wi, wp;  // issue cursor (kAhead chunks ahead) and dequantisation cursor
-    wi.start(a, n_units);
-    wp = wi;
-    const uint16_t* brow = nullptr;  // this thread's token row (pt < kBN)
-    const uint32_t* wq = nullptr;    // packed codes of row m0 of the issue unit
-    const uint32_t* wsb = nullptr;
-    int ldw = 0, lsb = 0;
-    auto unit_setup = [&]() {
-      const Tile& t = wi.t;
-      const bool sh = t.slot < 0;
-      const BlobLayout& B = sh ? a.LS : a.L;
-      const uint8_t* blob = sh ? a.shared_blob : a.pool + (uint64_t)t.slot * a.L.stride;
-      const int K = wi.nk * kBK;
-      ldw = K / 8;
-      lsb = K / a.G;
-      wq = reinterpret_cast<const uint32_t*>(blob + (DOWN ? B.d_q : B.gu_q)) +
-           (size_t)wi.m0 * ldw;
-      wsb = reinterpret_cast<const uint32_t*>(blob + (DOWN ? B.d_sb : B.gu_sb)) +
-            (size_t)wi.m0 * lsb;
-      brow = nullptr;
-      if (pt < t.ntok) {
-        if (DOWN) {
-          brow = a.h + (size_t)(t.hrow0 + pt) * a.hstride;
-        } else {
-          const int tok = sh ? t.pos0 + pt : a.perm[t.pos0 + pt] / a.k;
-          brow = a.x + (size_t)tok * a.H;
-        }
-      }
-    };
-    // copies of the chunk under the issue cursor into stage gi % kStages
-    auto issue = [&](uint32_t gi) {
-      const int s = gi % kStages;
-      const int c = wi.c;
-      if (brow) {
-        uint8_t* dst = S.b[s];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          ptx::cp_async16(dst + sw128_off(pt, ch), brow + c * kBK + ch * 8);
-      }
-      if (pt >= kBN) {
-        for (int v = pt - kBN; v < 3 * kBM; v += kProdThreads - kBN) {
-          if (v < 2 * kBM) {
-            const int r = v >> 1, half = v & 1;
-            ptx::cp_async16(S.raw[s] + r * 32 + half * 16,
-                            wq + (size_t)r * ldw + c * 8 + half * 4);
-          } else {
-            const int r = v - 2 * kBM;
-            const uint32_t* src = wsb + (size_t)r * lsb + (c * kBK) / a.G;
-            if (sbw == 2)
-              ptx::cp_async8(&S.rsb[s][2 * r], src);
-            else
-              ptx::cp_async4(&S.rsb[s][r], src);
-          }
-        }
-      }
-    };
-    bool wi_new = true;
-    uint32_t gi = 0, gp = 0;
-    bool abort = false;
-    for (int j = 0; j < kAhead; ++j) {
-      if (wi.live) {
-        if (wi_new) unit_setup();
-        issue(gi++);
-        wi_new = wi.next(a);
-      }
-      ptx::cp_async_commit();
-    }
-    while (wp.live) {
-      // copies for the chunk kAhead ahead, once the MMA has released its stage
-      if (wi.live && !abort) {
-        if (gi >= kStages &&
-            !wait_phase(&S.empty[gi % kStages], ((gi / kStages) + 1) & 1, S, a.err)) {
-          abort = true;
-        } else {
-          if (wi_new) unit_setup();
-          issue(gi++);
-          wi_new = wi.next(a);
-        }
-      }
-      ptx::cp_async_commit();
-      ptx::cp_async_wait<kAhead>();
-      // every producer's copies of chunk gp have landed, or the CTA aborts
-      if (ptx::bar_any(kBarProd, kProdThreads, abort || aborted(S))) break;
-      const int s = gp % kStages;
-      for (int u = pt; u < 2 * kBM; u += kProdThreads) {
-        const int r = u >> 1, half = u & 1;
-        const uint4 w = *reinterpret_cast<const uint4*>(S.raw[s] + r * 32 + half * 16);
-        const uint32_t sbv = sbw == 2 ? S.rsb[s][2 * r + half] : S.rsb[s][r];
-        uint4 o[4];
-        dequant32(w, sbv, o);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(S.a[s] + sw128_off(r, half * 4 + j)) = o[j];
-      }
+  } else if (warp < kDq0) {
+    // ------------------------------------------------------------ loaders
+    const int lw = warp - kLoad0;  // rows 4 (lw + 8 i) + lane / 8, i < 4
+    const int lt = lw * 32 + lane;
+    Walk<DOWN> w;
+    w.start(a, n_units);
+    const uint32_t* wsb = nullptr;  // scale/bias words of weight row m0
+    const uint16_t* bbase = DOWN ? a.h : a.x;
+    const int bpitch = DOWN ? a.hstride : a.H;
+    int lsb = 0, crow = 0, cblob = 0;
+    int rid[4];  // token-row ids of this lane's rows (-1: past the tile)
+    const CUtensorMap* cm = &cmap;
+    uint32_t g = 0, done = 0, gw = 0;  // chunks issued, chunks marked full, windows issued
+    uint32_t win_start[2] = {0, 0};    // first chunk of the last two windows
+    bool fresh = true;
+    // mark the oldest chunk in flight full once this lane's copies of it have landed
+    auto mark_oldest = [&]() {
       ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.full[s]);
-      ++gp;
-      wp.next(a);
+      ptx::mbar_arrive(&S.raw_full[done % kStages]);
+      ++done;
+    };
+    while (w.live) {
+      const int s = g % kStages;
+      if (g >= kStages && !wait_phase(&S.empty[s], ((g / kStages) + 1) & 1, S, a.err)) break;
+      if (fresh) {
+        const Tile& t = w.t;
+        const bool sh = t.slot < 0;
+        const BlobLayout& B = sh ? a.LS : a.L;
+        const uint8_t* blob = sh ? a.shared_blob : a.pool + (uint64_t)t.slot * a.L.stride;
+        lsb = w.nk * kBK / a.G;
+        wsb = reinterpret_cast<const uint32_t*>(blob + (DOWN ? B.d_sb : B.gu_sb)) +
+              (size_t)w.m0 * lsb;
+        cm = sh ? &cmap_sh : &cmap;
+        cblob = sh ? 0 : t.slot;
+        crow = w.m0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int n = 4 * (lw + kLoadWarps * i) + (lane >> 3);
+          rid[i] = n >= t.ntok ? -1
+                   : DOWN      ? t.hrow0 + n
+                   : sh        ? t.pos0 + n
+                               : a.perm[t.pos0 + n] / a.k;
+        }
+      }
+      const int c = w.c;
+      if (c % cpw == 0) {
+        // a new scale/bias window: words [c*64/G, +kSbWin) of the unit's 128 rows
+        const int wb = gw & 1;
+        if (gw >= 2) {
+          // the dequantisers free window gw-2 only after its last chunk is marked full
+          if (done < win_start[(gw - 1) & 1]) {
+            ptx::cp_async_wait_all();
+            while (done < g) mark_oldest();
+          }
+          if (!wait_phase(&S.sb_empty[wb], ((gw >> 1) + 1) & 1, S, a.err)) break;
+        }
+        win_start[wb] = g;
+        const int w0 = c * kBK / a.G, nw = min(kSbWin, lsb - w0);
+        for (int j = lt; j < kBM * nw; j += kLoadWarps * 32) {
+          const int row = j / nw, col = j - row * nw;
+          ptx::cp_async4(&S.sb[wb][row * kSbWin + col], wsb + (size_t)row * lsb + w0 + col);
+        }
+        ptx::cp_async_mbar_arrive(&S.sb_full[wb]);
+        ++gw;
+      }
+      uint8_t* st = S.raw[s];
+      if (lt == 0) {
+        ptx::mbar_arrive_expect_tx(&S.raw_full[s], kCodesBytes);
+        ptx::tma_load_3d(st + kCodesOff, cm, c * 8, crow, cblob, &S.raw_full[s]);
+      }
+      // token rows: 16-byte piece lane % 8 of rows 4 (lw + 8 i) + lane / 8
+      const int ch = lane & 7;
+      const uint16_t* bsrc = bbase + c * kBK + ch * 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (rid[i] >= 0)
+          ptx::cp_async16(st + sw128_off(4 * (lw + kLoadWarps * i) + (lane >> 3), ch),
+                          bsrc + (size_t)rid[i] * bpitch);
+      }
+      ptx::cp_async_commit();
+      ++g;
+      fresh = w.next(a);
+      if (g - done > kAhead) {
+        ptx::cp_async_wait<kAhead>();
+        mark_oldest();
+      }
     }
     ptx::cp_async_wait_all();
+    while (done < g) mark_oldest();
+  } else if (warp < kEpi0) {
+    // ------------------------------------------------------------ dequantisers
+    const int q = warp & 3;               // TMEM lane quarter = weight rows 32 q ..
+    const int kh = (warp - kDq0) >> 2;    // K-half of the chunk
+    const int r = q * 32 + lane;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + kACol0 + kh * 16;
+    Walk<DOWN> w;
+    w.start(a, n_units);
+    uint32_t g = 0, gw = 0;
+    while (w.live) {
+      const int sa = g % kStages;
+      const int c = w.c;
+      const int wb = (gw - (c % cpw == 0 ? 0 : 1)) & 1;  // window of this chunk
+      if (c % cpw == 0) {
+        if (!wait_phase(&S.sb_full[gw & 1], (gw >> 1) & 1, S, a.err)) break;
+        ++gw;
+      }
+      // the stage's copies have landed; the MMA that read its A tile last time is done
+      // (the loader waited for that before copying into the stage)
+      if (!wait_phase(&S.raw_full[sa], (g / kStages) & 1, S, a.err)) break;
+      ptx::tc_fence_after();
+      const uint8_t* st = S.raw[sa];
+      const uint4 cq = *reinterpret_cast<const uint4*>(st + kCodesOff + r * 32 + kh * 16);
+      const uint32_t sb = S.sb[wb][r * kSbWin + ((c * kBK + kh * 32) / a.G) % kSbWin];
+      uint32_t o[16];
+      dequant32(cq, sb, o);
+      ptx::tmem_st16(tq + sa * kACols, o);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.a_full[sa]);
+      ++g;
+      // the window's last chunk: its scale/bias buffer may be refilled
+      if ((c + 1) % cpw == 0 || c + 1 == w.nk) {
+        if (lane == 0) ptx::mbar_arrive(&S.sb_empty[wb]);
+      }
+      w.next(a);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                       // TMEM lane quarter
-    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0 .. 127
-    const int r = q * 32 + lane;                  // row of the unit
+    const int q = warp & 3;                   // TMEM lane quarter
+    const int et = threadIdx.x - kEpi0 * 32;  // 0 .. 127
+    float* xp = S.epi[q];                     // [16 columns][kEpiStride]
     Walk<DOWN> w;
     w.start(a, n_units);
     uint32_t ub = 0;
@@ -409,36 +465,53 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
       }
       const int buf = ub & 1;
       const bool ok = wait_phase(&S.acc_full[buf], (ub >> 1) & 1, S, a.err);
-      // one decision for all four warps (and the table is complete)
+      // one decision for all four warps (and the column table is complete)
       if (ptx::bar_any(kBarEpi, 128, !ok || aborted(S))) break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem + buf * kAccCols + ((uint32_t)(q * 32) << 16);
-      const int grow = w.m0 + r;
+      const int c = lane >> 1, hf = lane & 1;  // after the transpose: column, half
       for (int n0 = 0; n0 < t.ntok; n0 += 16) {
         float v[16];
         ptx::tmem_ld16(taddr + n0, v);
+        const int n = n0 + c;
         if (!DOWN) {
-          // gate row 2i in an even lane, up row 2i+1 in the next lane
-          uint16_t* hrow = a.h + (size_t)(t.hrow0 + n0) * a.hstride + (grow >> 1);
+          // gate row 2i in an even lane, up row 2i+1 in the next lane; the
+          // even lanes leave h for 16 features x 16 tokens, transposed
+          uint16_t* hx = reinterpret_cast<uint16_t*>(xp);  // [16 columns][16 features]
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            if ((lane & 1) == 0 && n0 + i < t.ntok)
-              hrow[(size_t)i * a.hstride] = f32_to_bf16_rne(silu_f(v[i]) * up);
+            if ((lane & 1) == 0) hx[i * 16 + (lane >> 1)] = f32_to_bf16_rne(silu_f(v[i]) * up);
           }
+          __syncwarp();
+          if (n < t.ntok) {
+            const uint4 hv = *reinterpret_cast<const uint4*>(hx + c * 16 + hf * 8);
+            *reinterpret_cast<uint4*>(a.h + (size_t)(t.hrow0 + n) * a.hstride + (w.m0 >> 1) +
+                                      q * 16 + hf * 8) = hv;
+          }
+          __syncwarp();
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = n0 + i;
-            if (n < t.ntok)
-              atomicAdd(a.y_acc + (size_t)S.tok_t[n] * a.H + grow, S.tok_w[n] * v[i]);
+          for (int i = 0; i < 16; ++i) xp[i * kEpiStride + lane] = v[i];
+          __syncwarp();
+          if (n < t.ntok) {
+            const float wt = S.tok_w[n];
+            float* dst = a.y_acc + (size_t)S.tok_t[n] * a.H + w.m0 + q * 32 + hf * 16;
+            const float* src = xp + c * kEpiStride + hf * 16;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 u = *reinterpret_cast<const float4*>(src + 4 * i);
+              atomicAdd(reinterpret_cast<float4*>(dst + 4 * i),
+                        make_float4(wt * u.x, wt * u.y, wt * u.z, wt * u.w));
+            }
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.acc_empty[buf]);
-      // the table is read by every warp before the next unit rewrites it
+      // the column table is read by every warp before the next unit rewrites it
       if (DOWN) ptx::bar_any(kBarEpi, 128, false);
       ++ub;
       w.next_unit(a);
@@ -548,16 +621,52 @@ cudaError_t prepare_prefill(const Ctx& c) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
 }
 
+// The tile list of the grouped GEMMs (after the permutation) and a zeroed
+// fp32 accumulator for y.
+cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& fa, cudaStream_t st,
+                                int* launches) {
+  const Dims& d = c.d;
+  const int T = fa.T, P = T * d.k;
+  build_tiles_kernel<<<1, 1024, 0, st>>>(c.ws.used, c.ws.n_used, c.ws.offsets, fa.table,
+                                         c.n_slots, T, P, reinterpret_cast<Tile*>(c.ws.tiles),
+                                         c.ws.n_tiles, prefill_max_tiles(d, T), c.err);
+  ++*launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return cudaMemsetAsync(c.ws.o, 0, (size_t)T * d.H * 4, st);
+}
+
+namespace {
+
+// Packed codes of `blobs` blobs: 3-D uint32 {K/8 words, rows, blobs}, box
+// 8 x 128 x 1 (the 64 codes of one K-chunk for 128 weight rows), no swizzle.
+bool encode_codes(CUtensorMap* m, const uint8_t* region, int K, int rows, int blobs,
+                  uint64_t blob_stride) {
+  const cuuint64_t dim[3] = {(cuuint64_t)K / 8, (cuuint64_t)rows, (cuuint64_t)blobs};
+  const cuuint64_t stride[2] = {(cuuint64_t)K / 2, blob_stride};
+  const cuuint32_t box[3] = {8, kBM, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3,
+                                const_cast<uint8_t*>(region), dim, stride, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t st,
                                    int* launches) {
   const Dims& d = c.d;
-  const int T = fa.T, P = T * d.k;
-  const int max_tiles = prefill_max_tiles(d, T);
-  Tile* tiles = reinterpret_cast<Tile*>(c.ws.tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(c.ws.used, c.ws.n_used, c.ws.offsets, fa.table,
-                                         c.n_slots, T, P, tiles, c.ws.n_tiles, max_tiles, c.err);
-  cudaError_t e = cudaMemsetAsync(c.ws.o, 0, (size_t)T * d.H * 4, st);
-  if (e != cudaSuccess) return e;
+  const int T = fa.T;
+  const int hstride = d.I > d.Is ? d.I : d.Is;
+  // tensor maps of the packed codes (host-side encoding, a few microseconds)
+  CUtensorMap gq, gq_sh, dq, dq_sh;
+  if (!encode_codes(&gq, c.pool + c.ex.gu_q, d.H, 2 * d.I, c.n_slots, c.ex.stride) ||
+      !encode_codes(&gq_sh, c.shared + c.sh.gu_q, d.H, 2 * d.Is, 1, c.sh.stride) ||
+      !encode_codes(&dq, c.pool + c.ex.d_q, d.I, d.H, c.n_slots, c.ex.stride) ||
+      !encode_codes(&dq_sh, c.shared + c.sh.d_q, d.Is, d.H, 1, c.sh.stride))
+    return cudaErrorInvalidValue;
   GemmArgs a;
   a.x = fa.x;
   a.perm = c.ws.perm;
@@ -567,7 +676,7 @@ cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t
   a.L = c.ex;
   a.shared_blob = c.shared;
   a.LS = c.sh;
-  a.tiles = tiles;
+  a.tiles = reinterpret_cast<const Tile*>(c.ws.tiles);
   a.n_tiles = c.ws.n_tiles;
   a.h = reinterpret_cast<uint16_t*>(c.ws.h);
   a.y_acc = c.ws.o;
@@ -577,15 +686,17 @@ cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t
   a.I = d.I;
   a.Is = d.Is;
   a.G = d.G;
-  a.hstride = d.I > d.Is ? d.I : d.Is;
-  a.nm = 2 * a.hstride / kBM;
+  a.hstride = hstride;
+  a.nm = 2 * hstride / kBM;
   a.test_stall = (c.test_flags & MOE_TEST_WAIT_TIMEOUT) ? 1 : 0;
-  grouped_gemm_kernel<false><<<c.num_sms, kThreads, kGemmSmem, st>>>(a);
+  grouped_gemm_kernel<false><<<c.num_sms, kThreads, kGemmSmem, st>>>(a, gq, gq_sh);
+  record_mark(c, MOE_MARK_GATEUP, st);
   a.nm = d.H / kBM;
-  grouped_gemm_kernel<true><<<c.num_sms, kThreads, kGemmSmem, st>>>(a);
+  grouped_gemm_kernel<true><<<c.num_sms, kThreads, kGemmSmem, st>>>(a, dq, dq_sh);
+  record_mark(c, MOE_MARK_DOWN, st);
   const int64_t n4 = (int64_t)T * d.H / 4;
   finalize_kernel<<<4 * c.num_sms, 256, 0, st>>>(c.ws.o, fa.y, n4);
-  *launches += 4;
+  *launches += 3;
   return cudaGetLastError();
 }
 

@@ -100,6 +100,180 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
   if (lane == 0) gate[t] = 1.0f / (1.0f + __expf(-gate_z[t]));
 }
 
+// ---------------------------------------------------------------- many tokens
+// For many tokens the logits are a GEMM [T x H] . [H x E]: register-tiled
+// fp32 FMAs, each CTA a tile of kTT tokens x kTE experts over a slice of H
+// (the slices split H when there are too few tiles to fill the GPU).
+// Summation structure of every logit: sequential FMAs over a chunk of kTK
+// terms from zero, the chunk sums of a slice added in order, the slice sums
+// added in order, then the prior, so a product passes through at most
+// D = kTK + H / kTK + slices + 1 roundings.  The bound uses twice
+// gamma_D times an upper bound of sum |x w| + |prior| (Higham, Accuracy and
+// Stability of Numerical Algorithms, Thm. 4.3); sum |x_h w_h| <= |x|_2 |w|_2
+// (Cauchy-Schwarz), with the 2-norms from router_norms_kernel.
+constexpr int kTT = 64, kTE = 128, kTK = 64;
+
+// Warp per row: rows r < T are tokens (2-norm bound and x . wsg), rows
+// T <= r < T + E are router rows (2-norm bound).  A warp's fp32 sum of
+// squares has depth H/256 * 8 + 5 <= 261, so multiplying its square root
+// by 1 + 2^-8 bounds the exact norm from above.
+__global__ void __launch_bounds__(256) router_norms_kernel(
+    const uint16_t* __restrict__ x, int T, const uint16_t* __restrict__ router_w, int E,
+    const uint16_t* __restrict__ wsg, int H, float* __restrict__ xnorm,
+    float* __restrict__ wnorm, float* __restrict__ gate_z) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (row >= T + E) return;
+  const bool tok = row < T;
+  const uint16_t* r = tok ? x + (size_t)row * H : router_w + (size_t)(row - T) * H;
+  float ss = 0.f, dz = 0.f;
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(r) + c);
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    uint32_t gw[4] = {0, 0, 0, 0};
+    if (tok) {
+      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(wsg) + c);
+      gw[0] = gv.x; gw[1] = gv.y; gw[2] = gv.z; gw[3] = gv.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a0 = bf16_lo(vw[q]), a1 = bf16_hi(vw[q]);
+      ss = fmaf(a0, a0, ss);
+      ss = fmaf(a1, a1, ss);
+      dz = fmaf(a0, bf16_lo(gw[q]), dz);
+      dz = fmaf(a1, bf16_hi(gw[q]), dz);
+    }
+  }
+  ss = warp_sum(ss);
+  dz = warp_sum(dz);
+  if (lane == 0) {
+    const float n = sqrtf(ss) * 1.00390625f;
+    if (tok) {
+      xnorm[row] = n;
+      gate_z[row] = dz;
+    } else {
+      wnorm[row - T] = n;
+    }
+  }
+}
+
+// Logit bound of the structure above.
+__device__ __forceinline__ void tile_logit_and_bound(float sum, float p, float xn, float wn,
+                                                     int H, int slices, float& l, float& b) {
+  const float scale =
+      2.0f * (float)(kTK + H / kTK + slices + 1) * 5.9604644775390625e-8f * 1.00390625f;
+  l = sum + p;
+  b = scale * (xn * wn + fabsf(p)) + kBoundFloor;
+}
+
+// blockIdx.z = slice of H (chunks [z * cps, (z + 1) * cps)).  With one slice
+// the kernel writes logits and bounds; otherwise the slice sums to
+// part[z][T][E] for router_slices_kernel.
+__global__ void __launch_bounds__(256, 2) router_tile_kernel(
+    const uint16_t* __restrict__ x, int T, const uint16_t* __restrict__ router_w,
+    const float* __restrict__ prior, int E, int H, int cps, const float* __restrict__ xnorm,
+    const float* __restrict__ wnorm, float* __restrict__ logits, float* __restrict__ bound,
+    float* __restrict__ part) {
+  __shared__ __align__(16) float xs[kTK][kTT];  // [h][token]
+  __shared__ __align__(16) float ws[kTK][kTE];  // [h][expert]
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // tokens 4 ty.., experts 8 tx..
+  float2 tot[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tot[i][j] = make_float2(0.f, 0.f);
+  const int kbeg = blockIdx.z * cps * kTK, kend = min(H, kbeg + cps * kTK);
+  for (int k0 = kbeg; k0 < kend; k0 += kTK) {
+    __syncthreads();
+    for (int i = tid; i < kTT * kTK / 8; i += 256) {
+      const int tt = i % kTT, hc = i / kTT;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t0 + tt < T) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0) + hc);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[hc * 8 + 2 * q][tt] = bf16_lo(vw[q]);
+        xs[hc * 8 + 2 * q + 1][tt] = bf16_hi(vw[q]);
+      }
+    }
+    for (int i = tid; i < kTE * kTK / 8; i += 256) {
+      const int ee = i % kTE, hc = i / kTE;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (e0 + ee < E)
+        v = __ldg(reinterpret_cast<const uint4*>(router_w + (size_t)(e0 + ee) * H + k0) + hc);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ws[hc * 8 + 2 * q][ee] = bf16_lo(vw[q]);
+        ws[hc * 8 + 2 * q + 1][ee] = bf16_hi(vw[q]);
+      }
+    }
+    __syncthreads();
+    float2 acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int h = 0; h < kTK; ++h) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
+      const float4 wa = *reinterpret_cast<const float4*>(&ws[h][tx * 8]);
+      const float4 wb = *reinterpret_cast<const float4*>(&ws[h][tx * 8 + 4]);
+      const float xi[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float2 wj[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
+                            make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[i][j] = __ffma2_rn(make_float2(xi[i], xi[i]), wj[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tot[i][j] = make_float2(tot[i][j].x + acc[i][j].x, tot[i][j].y + acc[i][j].y);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + tx * 8 + j;
+      if (e >= E) continue;
+      const float sum = (j & 1) ? tot[i][j >> 1].y : tot[i][j >> 1].x;
+      if (gridDim.z > 1) {
+        part[((size_t)blockIdx.z * T + t) * E + e] = sum;
+      } else {
+        float l, b;
+        tile_logit_and_bound(sum, prior ? prior[e] : 0.f, xnorm[t], wnorm[e], H, 1, l, b);
+        logits[(size_t)t * E + e] = l;
+        bound[(size_t)t * E + e] = b;
+      }
+    }
+  }
+}
+
+// Sum of the slice sums in slice order, then the prior.
+__global__ void router_slices_kernel(const float* __restrict__ part, int slices, int T, int E,
+                                     int H, const float* __restrict__ prior,
+                                     const float* __restrict__ xnorm,
+                                     const float* __restrict__ wnorm, float* __restrict__ logits,
+                                     float* __restrict__ bound) {
+  const int64_t n = (int64_t)T * E;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float sum = part[i];
+    for (int z = 1; z < slices; ++z) sum += part[(size_t)z * n + i];
+    const int t = (int)(i / E), e = (int)(i - (int64_t)t * E);
+    float l, b;
+    tile_logit_and_bound(sum, prior ? prior[e] : 0.f, xnorm[t], wnorm[e], H, slices, l, b);
+    logits[i] = l;
+    bound[i] = b;
+  }
+}
+
 // topk_kernel with the per-lane list length fitting E.
 cudaError_t launch_topk_any(const float* logits, const float* bound, const float* gate_z,
                             const uint16_t* x, const uint16_t* router_w, const float* prior,
@@ -175,6 +349,31 @@ cudaError_t launch_router_any(const uint16_t* x, int T, const uint16_t* router_w
 }  // namespace
 
 cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches) {
+  if (a.T >= kTileRouterMinT) {
+    const int rows = a.T + c.d.E;
+    router_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a.x, a.T, c.router_w, c.d.E,
+                                                       c.shared_gate_w, c.d.H, c.ws.xnorm,
+                                                       c.ws.wnorm, c.ws.gate_z);
+    const int tiles = ((a.T + kTT - 1) / kTT) * ((c.d.E + kTE - 1) / kTE);
+    const int chunks = c.d.H / kTK;
+    // slices of H so that about two CTAs per SM are busy (one slice when the tiles suffice)
+    int slices = max(1, min(chunks, (2 * c.num_sms) / tiles));
+    if ((int64_t)slices * a.T * c.d.E > tile_router_part_floats(c.num_sms)) slices = 1;
+    const int cps = (chunks + slices - 1) / slices;
+    slices = (chunks + cps - 1) / cps;
+    dim3 grid((a.T + kTT - 1) / kTT, (c.d.E + kTE - 1) / kTE, slices);
+    router_tile_kernel<<<grid, 256, 0, st>>>(a.x, a.T, c.router_w, c.router_bias, c.d.E, c.d.H,
+                                             cps, c.ws.xnorm, c.ws.wnorm, c.ws.logits,
+                                             c.ws.bound, c.ws.rpart);
+    *launches += 2;
+    if (slices > 1) {
+      router_slices_kernel<<<2 * c.num_sms, 256, 0, st>>>(c.ws.rpart, slices, a.T, c.d.E, c.d.H,
+                                                          c.router_bias, c.ws.xnorm, c.ws.wnorm,
+                                                          c.ws.logits, c.ws.bound);
+      ++*launches;
+    }
+    return cudaGetLastError();
+  }
   ++*launches;
   return launch_router_any(a.x, a.T, c.router_w, c.router_bias, c.shared_gate_w, c.d.E, c.d.H,
                            c.ws.logits, c.ws.bound, c.ws.gate_z, st);

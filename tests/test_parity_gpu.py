@@ -79,14 +79,16 @@ def test_k_equals_E_dense_mixture():
 
 
 # ------------------------------------------------------------------ exact routing
-def test_exact_ties_go_to_lowest_index():
-    """Identical router rows: every logit ties; the GPU must take experts 0..k-1."""
+@pytest.mark.parametrize("T", [6, 40])
+def test_exact_ties_go_to_lowest_index(T):
+    """Identical router rows: every logit ties; the GPU must take experts 0..k-1
+    (T = 40 goes through the tiled many-token router)."""
     W = _weights(W0)
     W["router_w"] = np.repeat(W["router_w"][:1], W0.E, axis=0)
-    x = _x(W0, 6)
-    L = U.layer(W0.shape, W, max_T=6)
+    x = _x(W0, T)
+    L = U.layer(W0.shape, W, max_T=T)
     out = U.run(L, x)
-    assert out["topk_idx"].tolist() == [list(range(W0.k))] * 6
+    assert out["topk_idx"].tolist() == [list(range(W0.k))] * T
     ref = O.moe_block(x, W, W0.k, W0.G)
     U.assert_parity(out, ref, what="ties")
 
@@ -105,14 +107,15 @@ def test_near_ties_one_ulp_apart():
     U.assert_parity(U.run(L, x), ref, what="near ties")
 
 
-def test_duplicate_rows_with_prior():
+@pytest.mark.parametrize("T", [12, 100])
+def test_duplicate_rows_with_prior(T):
     shape = synth.Shape(E=64, k=6, H=256, I=64, Is=64, G=32)
     W = synth.layer_weights(0, 0, 11, shape, zipf_s=0.0)
     rw = W["router_w"]
     rw[10:20] = rw[3]
     W["router_bias"] = np.zeros(shape.E, np.float32)
-    x = synth.tokens(0, 0, 11, 0, 12, shape.H)
-    L = U.layer(shape, W, max_T=12)
+    x = synth.tokens(0, 0, 11, 0, T, shape.H)
+    L = U.layer(shape, W, max_T=T)
     ref = O.moe_block(x, W, shape.k, shape.G)
     U.assert_parity(U.run(L, x), ref, what="duplicate rows")
 
