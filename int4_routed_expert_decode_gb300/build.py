@@ -64,7 +64,7 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int | None =
         return LIB
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=HERE)
     os.close(fd)
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         os.unlink(tmp)

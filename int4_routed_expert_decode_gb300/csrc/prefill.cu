@@ -638,6 +638,27 @@ cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& fa, cudaStream_t st
 
 namespace {
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that
+// the library does not link the driver library (it loads without a GPU).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
 // Packed codes of `blobs` blobs: 3-D uint32 {K/8 words, rows, blobs}, box
 // 8 x 128 x 1 (the 64 codes of one K-chunk for 128 weight rows), no swizzle.
 bool encode_codes(CUtensorMap* m, const uint8_t* region, int K, int rows, int blobs,
@@ -646,7 +667,9 @@ bool encode_codes(CUtensorMap* m, const uint8_t* region, int K, int rows, int bl
   const cuuint64_t stride[2] = {(cuuint64_t)K / 2, blob_stride};
   const cuuint32_t box[3] = {8, kBM, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3,
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3,
                                 const_cast<uint8_t*>(region), dim, stride, box, es,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
