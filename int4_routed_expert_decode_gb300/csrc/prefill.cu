@@ -76,6 +76,7 @@ constexpr int kCodesOff = kTileBytes;       // in a raw stage: 4 KiB of codes
 constexpr int kCodesBytes = kBM * 32;
 constexpr int kRawStride = kTileBytes + kCodesBytes;  // 20 KiB, 1 KiB aligned
 constexpr int kSbWin = 32;                  // scale/bias words per row in a window
+constexpr int kSbPitch = kSbWin + 1;        // row pitch in the window buffer (bank spread)
 constexpr int kEpiStride = 36;              // floats per transposed column (bank spread)
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr int kBarEpi = 1;                  // named barrier of the epilogue warps
@@ -111,7 +112,7 @@ struct GemmArgs {
 
 struct Smem {
   uint8_t raw[kStages][kRawStride];  // token rows (swizzled), codes
-  uint32_t sb[2][kBM * kSbWin];      // scale/bias windows [row][word]
+  uint32_t sb[2][kBM * kSbPitch];    // scale/bias windows [row][word]
   float epi[4][16 * kEpiStride];     // per epilogue warp: 16 columns x 32 rows
   uint64_t raw_full[kStages], a_full[kStages], empty[kStages], sb_full[2], sb_empty[2];
   uint64_t acc_full[2], acc_empty[2], drain;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
   // scale/bias windows: up to kSbWin group words per row, i.e. cpw chunks
   const int cpw = kSbWin * a.G / kBK;
+  const int lg = 31 - __clz(a.G);  // log2 of the group size (32, 64 or 128)
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w0 = c * kBK / a.G, nw = min(kSbWin, lsb - w0);
         for (int j = lt; j < kBM * nw; j += kLoadWarps * 32) {
           const int row = j / nw, col = j - row * nw;
-          ptx::cp_async4(&S.sb[wb][row * kSbWin + col], wsb + (size_t)row * lsb + w0 + col);
+          ptx::cp_async4(&S.sb[wb][row * kSbPitch + col], wsb + (size_t)row * lsb + w0 + col);
         }
         ptx::cp_async_mbar_arrive(&S.sb_full[wb]);
         ++gw;
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint8_t* st = S.raw[sa];
       const uint4 cq = *reinterpret_cast<const uint4*>(st + kCodesOff + r * 32 + kh * 16);
-      const uint32_t sb = S.sb[wb][r * kSbWin + ((c * kBK + kh * 32) / a.G) % kSbWin];
+      const uint32_t sb = S.sb[wb][r * kSbPitch + (((c * kBK + kh * 32) >> lg) & (kSbWin - 1))];
       uint32_t o[16];
       dequant32(cq, sb, o);
       ptx::tmem_st16(tq + sa * kACols, o);
