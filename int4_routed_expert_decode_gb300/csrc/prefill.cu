@@ -327,21 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t* bbase = DOWN ? a.h : a.x;
     const int bpitch = DOWN ? a.hstride : a.H;
     int lsb = 0, crow = 0, cblob = 0;
-    int rid[4];  // token-row ids of this lane's rows (-1: past the tile)
+    int rid[4] = {-1, -1, -1, -1};  // token-row ids of this lane's rows (-1: past the tile)
     const CUtensorMap* cm = &cmap;
     uint32_t g = 0, done = 0, gw = 0;  // chunks issued, chunks marked full, windows issued
     uint32_t win_start[2] = {0, 0};    // first chunk of the last two windows
-    bool fresh = true;
+    bool ok = true;
     // mark the oldest chunk in flight full once this lane's copies of it have landed
     auto mark_oldest = [&]() {
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&S.raw_full[done % kStages]);
       ++done;
     };
-    while (w.live) {
-      const int s = g % kStages;
-      if (g >= kStages && !wait_phase(&S.empty[s], ((g / kStages) + 1) & 1, S, a.err)) break;
-      if (fresh) {
+    const int ch = lane & 7;  // 16-byte piece of a token row
+    while (ok && w.live) {
+      {
         const Tile& t = w.t;
         const bool sh = t.slot < 0;
         const BlobLayout& B = sh ? a.LS : a.L;
@@ -361,9 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : a.perm[t.pos0 + n] / a.k;
         }
       }
-      const int c = w.c;
-      if (c % cpw == 0) {
-        // a new scale/bias window: words [c*64/G, +kSbWin) of the unit's 128 rows
+      for (int c0 = 0; ok && c0 < w.nk; c0 += cpw) {
+        // a new scale/bias window: words [c0*64/G, +kSbWin) of the unit's 128 rows
         const int wb = gw & 1;
         if (gw >= 2) {
           // the dequantisers free window gw-2 only after its last chunk is marked full
@@ -371,38 +369,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::cp_async_wait_all();
             while (done < g) mark_oldest();
           }
-          if (!wait_phase(&S.sb_empty[wb], ((gw >> 1) + 1) & 1, S, a.err)) break;
+          if (!wait_phase(&S.sb_empty[wb], ((gw >> 1) + 1) & 1, S, a.err)) {
+            ok = false;
+            break;
+          }
         }
         win_start[wb] = g;
-        const int w0 = c * kBK / a.G, nw = min(kSbWin, lsb - w0);
+        const int w0 = c0 * kBK / a.G, nw = min(kSbWin, lsb - w0);
         for (int j = lt; j < kBM * nw; j += kLoadWarps * 32) {
           const int row = j / nw, col = j - row * nw;
           ptx::cp_async4(&S.sb[wb][row * kSbPitch + col], wsb + (size_t)row * lsb + w0 + col);
         }
         ptx::cp_async_mbar_arrive(&S.sb_full[wb]);
         ++gw;
-      }
-      uint8_t* st = S.raw[s];
-      if (lt == 0) {
-        ptx::mbar_arrive_expect_tx(&S.raw_full[s], kCodesBytes);
-        ptx::tma_load_3d(st + kCodesOff, cm, c * 8, crow, cblob, &S.raw_full[s]);
-      }
-      // token rows: 16-byte piece lane % 8 of rows 4 (lw + 8 i) + lane / 8
-      const int ch = lane & 7;
-      const uint16_t* bsrc = bbase + c * kBK + ch * 8;
+        const int c1 = min(w.nk, c0 + cpw);
+        for (int c = c0; c < c1; ++c) {
+          const int s = g % kStages;
+          if (g >= kStages && !wait_phase(&S.empty[s], ((g / kStages) + 1) & 1, S, a.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = S.raw[s];
+          if (lt == 0) {
+            ptx::mbar_arrive_expect_tx(&S.raw_full[s], kCodesBytes);
+            ptx::tma_load_3d(st + kCodesOff, cm, c * 8, crow, cblob, &S.raw_full[s]);
+          }
+          // token rows: piece ch of rows 4 (lw + 8 i) + lane / 8
+          const uint16_t* bsrc = bbase + c * kBK + ch * 8;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (rid[i] >= 0)
-          ptx::cp_async16(st + sw128_off(4 * (lw + kLoadWarps * i) + (lane >> 3), ch),
-                          bsrc + (size_t)rid[i] * bpitch);
+          for (int i = 0; i < 4; ++i) {
+            if (rid[i] >= 0)
+              ptx::cp_async16(st + sw128_off(4 * (lw + kLoadWarps * i) + (lane >> 3), ch),
+                              bsrc + (size_t)rid[i] * bpitch);
+          }
+          ptx::cp_async_commit();
+          ++g;
+          if (g - done > kAhead) {
+            ptx::cp_async_wait<kAhead>();
+            mark_oldest();
+          }
+        }
       }
-      ptx::cp_async_commit();
-      ++g;
-      fresh = w.next(a);
-      if (g - done > kAhead) {
-        ptx::cp_async_wait<kAhead>();
-        mark_oldest();
-      }
+      w.next_unit(a);
     }
     ptx::cp_async_wait_all();
     while (done < g) mark_oldest();
@@ -415,34 +423,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walk<DOWN> w;
     w.start(a, n_units);
     uint32_t g = 0, gw = 0;
-    while (w.live) {
-      const int sa = g % kStages;
-      const int c = w.c;
-      const int wb = (gw - (c % cpw == 0 ? 0 : 1)) & 1;  // window of this chunk
-      if (c % cpw == 0) {
-        if (!wait_phase(&S.sb_full[gw & 1], (gw >> 1) & 1, S, a.err)) break;
+    bool ok = true;
+    while (ok && w.live) {
+      for (int c0 = 0; c0 < w.nk; c0 += cpw) {  // scale/bias windows of the unit
+        const int wb = gw & 1;
+        if (!wait_phase(&S.sb_full[wb], (gw >> 1) & 1, S, a.err)) {
+          ok = false;
+          break;
+        }
         ++gw;
-      }
-      // the stage's copies have landed; the MMA that read its A tile last time is done
-      // (the loader waited for that before copying into the stage)
-      if (!wait_phase(&S.raw_full[sa], (g / kStages) & 1, S, a.err)) break;
-      ptx::tc_fence_after();
-      const uint8_t* st = S.raw[sa];
-      const uint4 cq = *reinterpret_cast<const uint4*>(st + kCodesOff + r * 32 + kh * 16);
-      const uint32_t sb = S.sb[wb][r * kSbPitch + (((c * kBK + kh * 32) >> lg) & (kSbWin - 1))];
-      uint32_t o[16];
-      dequant32(cq, sb, o);
-      ptx::tmem_st16(tq + sa * kACols, o);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.a_full[sa]);
-      ++g;
-      // the window's last chunk: its scale/bias buffer may be refilled
-      if ((c + 1) % cpw == 0 || c + 1 == w.nk) {
+        const uint32_t* sbrow = &S.sb[wb][r * kSbPitch];
+        const int c1 = min(w.nk, c0 + cpw);
+        for (int c = c0; c < c1; ++c) {
+          const int sa = g % kStages;
+          // the stage's copies have landed; the MMA that read its A tile last
+          // time is done (the loader waited for that before copying)
+          if (!wait_phase(&S.raw_full[sa], (g / kStages) & 1, S, a.err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint8_t* st = S.raw[sa];
+          const uint4 cq = *reinterpret_cast<const uint4*>(st + kCodesOff + r * 32 + kh * 16);
+          const uint32_t sb = sbrow[((c * kBK + kh * 32) >> lg) & (kSbWin - 1)];
+          uint32_t o[16];
+          dequant32(cq, sb, o);
+          ptx::tmem_st16(tq + sa * kACols, o);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&S.a_full[sa]);
+          ++g;
+        }
+        if (!ok) break;
+        // the window's last chunk is done: its scale/bias buffer may be refilled
         if (lane == 0) ptx::mbar_arrive(&S.sb_empty[wb]);
       }
-      w.next(a);
+      w.next_unit(a);
     }
   } else {
     // ------------------------------------------------------------ epilogue
