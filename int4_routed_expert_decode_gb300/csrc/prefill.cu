@@ -84,6 +84,7 @@ constexpr int kBarEpi = 1;                  // named barrier of the epilogue war
 static_assert(kDqWarps == 8, "two dequantising warps per TMEM lane quarter");
 static_assert(kACol0 + kStages * kACols <= kTmemCols, "TMEM budget");
 static_assert(kAhead < kStages, "the loader must mark a stage full before it needs that stage again");
+static_assert(kBK == 64 && kACols == 32, "the MMA issue loop unrolls 4 K-steps of 16");
 
 struct Tile {
   int slot;   // expert slot, or -1 for the shared expert
@@ -284,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // test hook: no arrival precedes the final commit, so this wait runs out
       if (a.test_stall) ok = wait_phase(&S.drain, 0, S, a.err);
+      // B descriptors: stage s starts kRawStride bytes after stage s-1 (the start
+      // address field counts 16-byte units); a K-step of 16 advances 32 bytes
+      const uint64_t bdesc0 = sw128_desc(ptx::smem_u32(S.raw[0]));
+      const uint32_t acol0 = tmem + kACol0;
       while (ok && w.live) {
         const int nmma = max(16, (w.t.ntok + 15) & ~15);
         const uint32_t idesc = idesc_bf16(kBM, nmma);
@@ -292,19 +297,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d = tmem + buf * kAccCols;
         do {
-          const int s = g % kStages;
-          const uint32_t par = (g / kStages) & 1;
-          if (!wait_phase(&S.a_full[s], par, S, a.err) || !wait_phase(&S.raw_full[s], par, S, a.err)) {
+          const uint32_t s = g % kStages;
+          // the dequantisers arrive only after the stage's copies have landed
+          if (!wait_phase(&S.a_full[s], (g / kStages) & 1, S, a.err)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t at = tmem + kACol0 + s * kACols;
-          const uint32_t bb = ptx::smem_u32(S.raw[s]);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            ptx::tc_mma_f16_ta(d, at + kk * 8, sw128_desc(bb + kk * 32), idesc,
-                               (w.c > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t at = acol0 + s * kACols;
+          const uint64_t bd = bdesc0 + (uint64_t)(s * (kRawStride >> 4));
+          ptx::tc_mma_f16_ta(d, at, bd, idesc, w.c > 0 ? 1u : 0u);
+          ptx::tc_mma_f16_ta(d, at + 8, bd + 2, idesc, 1u);
+          ptx::tc_mma_f16_ta(d, at + 16, bd + 4, idesc, 1u);
+          ptx::tc_mma_f16_ta(d, at + 24, bd + 6, idesc, 1u);
           ptx::tc_commit(&S.empty[s]);
           ++g;
         } while (!w.next(a));
