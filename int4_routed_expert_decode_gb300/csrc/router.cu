@@ -176,7 +176,9 @@ __global__ void __launch_bounds__(256, 2) router_tile_kernel(
   __shared__ __align__(16) float xs[kTK][kTT];  // [h][token]
   __shared__ __align__(16) float ws[kTK][kTE];  // [h][expert]
   const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // tokens 4 ty.., experts 8 tx..
+  // thread: tokens 4 ty .. 4 ty + 3, experts 4 tx .. 4 tx + 3 and 64 + 4 tx .. 64 + 4 tx + 3
+  // (consecutive lanes read consecutive 16-byte words of a shared-memory row)
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   float2 tot[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -217,8 +219,8 @@ __global__ void __launch_bounds__(256, 2) router_tile_kernel(
 #pragma unroll 4
     for (int h = 0; h < kTK; ++h) {
       const float4 xv = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
-      const float4 wa = *reinterpret_cast<const float4*>(&ws[h][tx * 8]);
-      const float4 wb = *reinterpret_cast<const float4*>(&ws[h][tx * 8 + 4]);
+      const float4 wa = *reinterpret_cast<const float4*>(&ws[h][tx * 4]);
+      const float4 wb = *reinterpret_cast<const float4*>(&ws[h][64 + tx * 4]);
       const float xi[4] = {xv.x, xv.y, xv.z, xv.w};
       const float2 wj[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
                             make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(256, 2) router_tile_kernel(
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int e = e0 + tx * 8 + j;
+      const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
       if (e >= E) continue;
       const float sum = (j & 1) ? tot[i][j >> 1].y : tot[i][j >> 1].x;
       if (gridDim.z > 1) {
