@@ -499,13 +499,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld16(taddr + n0, v);
         const int n = n0 + c;
         if (!DOWN) {
-          // gate row 2i in an even lane, up row 2i+1 in the next lane; the
-          // even lanes leave h for 16 features x 16 tokens, transposed
+          // gate row 2i in an even lane, up row 2i+1 in the next lane: the
+          // even lane takes columns 0-7 of the pair, the odd lane columns
+          // 8-15, and both leave h for 16 features x 16 tokens, transposed
           uint16_t* hx = reinterpret_cast<uint16_t*>(xp);  // [16 columns][16 features]
+          const bool odd = lane & 1;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float up = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            if ((lane & 1) == 0) hx[i * 16 + (lane >> 1)] = f32_to_bf16_rne(silu_f(v[i]) * up);
+          for (int i = 0; i < 8; ++i) {
+            // even lane sends its column 8+i (gate), odd lane its column i (up)
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
+            const float gt = odd ? other : v[i];
+            const float up = odd ? v[8 + i] : other;
+            const int col = odd ? 8 + i : i;
+            hx[col * 16 + (lane >> 1)] = f32_to_bf16_rne(silu_f(gt) * up);
           }
           __syncwarp();
           if (n < t.ntok) {
