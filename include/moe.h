@@ -150,7 +150,7 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
 /* Kernel path of moe_forward.  MOE_PATH_AUTO uses the fused single-launch
  * decode kernel for T = 1 when the sizes allow it (hidden in {256, 512,
  * 1024, 2048}, inter == shared_inter <= 1024), the tensor-core grouped GEMMs
- * for T > 64 when hidden, 2*inter and 2*shared_inter are multiples of 128,
+ * for T >= 2 when hidden, 2*inter and 2*shared_inter are multiples of 128,
  * and the general kernels otherwise.  MOE_PATH_DECODE insists on the fused
  * kernel and MOE_PATH_PREFILL on the grouped GEMMs (any T >= 1); either
  * returns MOE_ERR_UNSUPPORTED if its sizes do not allow it.

@@ -374,8 +374,10 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   if (c.path == MOE_PATH_PREFILL && !prefill_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
                    "the prefill path needs hidden and 2*inter multiples of 128");
+  // measured on GB300: from two tokens on, the grouped GEMMs beat the general
+  // CUDA-core kernels (at T = 64 by 30x), so AUTO uses them whenever the sizes allow
   const bool use_prefill =
-      c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > kDecodeMaxT);
+      c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > 1);
   cudaError_t e;
   record_mark(c, MOE_MARK_START, st);
   if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE)) {

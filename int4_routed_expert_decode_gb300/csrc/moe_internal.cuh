@@ -12,7 +12,6 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr int kMaxH = 8192;
 constexpr int kMaxInter = 4096;
-constexpr int kDecodeMaxT = 64;
 constexpr int kSyncWords = 1;  // counters of the fused decode kernel
 constexpr int kTileRouterMinT = 16;  // from this many tokens the router is a tiled GEMM
 // Floats of the router's slice sums: the slices are only used while
