@@ -12,7 +12,8 @@
 //   P1  router logits with their rigorous error bounds, and the shared
 //       expert's gate/up + SwiGLU (neither depends on routing);
 //       -- grid barrier --
-//   P2  every CTA selects the top-k itself (exact order, routing_common.cuh),
+//   P2  every CTA selects the top-k itself with all its warps (exact order,
+//       routing_common.cuh),
 //       then bulk-copies its share of the selected experts' gate/up rows and
 //       its rows of their down projections;
 //   P3  gate/up + SwiGLU of the selected experts from shared memory;
@@ -45,7 +46,7 @@ constexpr uint32_t kMbarTries = 1u << 22;  // mbarrier try_waits
 constexpr int kNumMbar = 10;               // 0: P0 weights, 1..8: P3 warps, 9: P4 down rows
 
 struct FusedSmem {  // byte offsets into dynamic shared memory
-  uint32_t mbar, misc, topk, p1, sd, p3, p3_warp, p4, p4_expert, p4_sb, ypart, total;
+  uint32_t mbar, misc, topk, lists, p1, sd, p3, p3_warp, p4, p4_expert, p4_sb, ypart, total;
   uint32_t p1_max;    // bytes reserved for router + shared gate/up rows
   uint32_t seg_max;   // row-pairs per warp segment (max)
   uint32_t nrow_max;  // P4 rows per CTA (max)
@@ -295,26 +296,32 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   grid_barrier(a.bar, nC + a.bar_extra, a.err);
 
   // ---------------------------------------------------------------- P2
-  if (warp == 0) {
+  {
+    const float gz = __ldcg(a.gate_z);  // issued early: its latency overlaps the selection
     int* sel_idx;
     float* sel_val;
-    topk_select_warp<MAXV>(a.logits, a.bound, E, k, a.x, a.router_w, a.prior, H,
-                           sm + a.sm.topk, &sel_idx, &sel_val);
-    const float w = renormalised_weight(sel_val, k);
-    if (lane < k) {
-      const int e = sel_idx[lane];
-      const int slot = a.table ? __ldg(a.table + e) : e;
-      const bool ok = slot >= 0 && slot < a.n_slots;
-      s_idx[lane] = e;
-      s_w[lane] = w;
-      s_slot[lane] = ok ? slot : -1;
-      if (!ok && c == 0) record_error(a.err, MOE_ERR_SLOT);
-      if (c == 0) {
-        a.topk_idx[lane] = e;
-        a.topk_w[lane] = w;
+    topk_select_block<MAXV / kWarps>(PlainLogits{a.logits, a.bound}, E, k, a.x, a.router_w,
+                                     a.prior, H, sm + a.sm.topk,
+                                     reinterpret_cast<uint2*>(sm + a.sm.lists),
+                                     reinterpret_cast<float*>(sm + a.sm.lists + (size_t)E * 8),
+                                     &sel_idx, &sel_val);
+    if (warp == 0) {
+      const float w = renormalised_weight(sel_val, k);
+      if (lane < k) {
+        const int e = sel_idx[lane];
+        const int slot = a.table ? __ldg(a.table + e) : e;
+        const bool ok = slot >= 0 && slot < a.n_slots;
+        s_idx[lane] = e;
+        s_w[lane] = w;
+        s_slot[lane] = ok ? slot : -1;
+        if (!ok && c == 0) record_error(a.err, MOE_ERR_SLOT);
+        if (c == 0) {
+          a.topk_idx[lane] = e;
+          a.topk_w[lane] = w;
+        }
       }
+      if (lane == 0) *s_g = 1.0f / (1.0f + __expf(-gz));
     }
-    if (lane == 0) *s_g = 1.0f / (1.0f + __expf(-__ldcg(a.gate_z)));
   }
   __syncthreads();
 
@@ -426,16 +433,29 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       const uint8_t* sbbase = shared ? sd_sb + dsb_off
                                      : sm + a.sm.p4 + (size_t)(in_range ? j : 0) * a.sm.p4_expert +
                                            a.sm.p4_sb + dsb_off;
-      for (int rl = 0; rl < nrow; ++rl) {
-        float v = 0.f;
-        if (valid) {
-          const uint4 q = reinterpret_cast<const uint4*>(qbase + (size_t)rl * (I / 2))[sub];
-          const uint32_t sbw =
-              reinterpret_cast<const uint32_t*>(sbbase + (size_t)rl * IG * 4)[sub * 32 / G];
-          v = chunk_term(q, sbw, hr, hsum);
+      // four rows at a time: their chunk terms and group sums are independent
+      for (int rb = 0; rb < nrow; rb += 4) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rl = rb + u;
+          v[u] = 0.f;
+          if (valid && rl < nrow) {
+            const uint4 q = reinterpret_cast<const uint4*>(qbase + (size_t)rl * (I / 2))[sub];
+            const uint32_t sbw =
+                reinterpret_cast<const uint32_t*>(sbbase + (size_t)rl * IG * 4)[sub * 32 / G];
+            v[u] = chunk_term(q, sbw, hr, hsum);
+          }
         }
-        v = group_sum(v, lpu);
-        if (in_range && sub == 0) ypart[rl * (k + 1) + j] = v;
+        for (int o = lpu >> 1; o > 0; o >>= 1) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], o);
+        }
+        if (in_range && sub == 0) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (rb + u < nrow) ypart[(rb + u) * (k + 1) + j] = v[u];
+        }
       }
     }
   }
@@ -463,6 +483,7 @@ bool plan_smem(const Ctx& c, int nC, FusedSmem& s) {
   s.mbar = take(kNumMbar * 8);
   s.misc = take(512);
   s.topk = take((uint32_t)topk_warp_smem(E));
+  s.lists = take((uint32_t)E * 8 + kWarps * 4);
   // P1: worst CTA of router rows * 2H + shared features * (H + 8H/G)
   const int U1 = E + I + 1;
   uint32_t p1 = 0;

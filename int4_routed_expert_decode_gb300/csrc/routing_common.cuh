@@ -457,12 +457,89 @@ __device__ void topk_select_warp(const float* lrow, const float* brow, int E, in
                              sel_idx_out, sel_val_out);
 }
 
+// The same selection by all `nw` warps of a CTA (E <= nw * 32 * V), for
+// latency: warp w sorts experts [32 V w, 32 V (w + 1)) across its lanes
+// (best first; ties to the lower id) into `lists` (shared memory, E entries
+// of (key, id)), then warp 0 merges the nw lists -- lane l < nw holds the
+// head of list l -- with the closing rule and the run resolution of
+// topk_select_warp_src, so the result is identical.  Every thread of the CTA
+// calls; the selection is complete on return (one __syncthreads inside, none
+// after: sel_idx / sel_val are written by warp 0).
+//   smem: topk_warp_smem(E) bytes; lists: E * 8 bytes; bmx: nw floats.
+template <int V, typename Src>
+__device__ void topk_select_block(const Src& src, int E, int k, const uint16_t* xt,
+                                  const uint16_t* router_w, const float* prior, int H,
+                                  uint8_t* smem, uint2* lists, float* bmx, int** sel_idx_out,
+                                  float** sel_val_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int* sel_idx = reinterpret_cast<int*>(smem);
+  float* sel_val = reinterpret_cast<float*>(smem + (size_t)E * 4);
+  uint32_t* cache = reinterpret_cast<uint32_t*>(smem + (size_t)E * 8);
+  uint32_t* scratch = cache + kRunCache * kDigits;
+  *sel_idx_out = sel_idx;
+  *sel_val_out = sel_val;
+  constexpr int L = 32 * V;  // list length
+  uint32_t key[V];
+  int id[V];
+  uint32_t bm = 0;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int e = warp * L + lane * V + v;
+    float l = 0.f, bnd = 0.f;
+    if (e < E) src.get(e, l, bnd);
+    if (l != l) l = -INFINITY;
+    key[v] = (e < E) ? f32_key(l) : 0u;
+    id[v] = (e < E) ? e : 0x7FFFFFFF;
+    if (e < E) bm = max(bm, __float_as_uint(bnd));
+  }
+  bm = __reduce_max_sync(0xffffffffu, bm);
+  warp_bitonic_sort<V>(key, id);
+  if (warp * L < E) {
+#pragma unroll
+    for (int v = 0; v < V; ++v) lists[warp * L + lane * V + v] = make_uint2(key[v], (uint32_t)id[v]);
+  }
+  if (lane == 0) bmx[warp] = __uint_as_float(bm);
+  __syncthreads();
+  if (warp != 0) return;
+  float thr = 0.f;
+  for (int w = 0; w < nw; ++w) thr = fmaxf(thr, bmx[w]);
+  thr *= 2.0f;
+  const int nl = (E + L - 1) / L;  // lists that hold experts
+  int pos = 0;
+  uint2 head = (lane < nl) ? lists[lane * L] : make_uint2(0u, 0x7FFFFFFFu);
+  const int len = (lane < nl) ? min(L, E - lane * L) : 0;
+  int n = 0;
+  while (n < E) {
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, head.x);
+    if (kmax == 0u) break;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, head.x == kmax ? head.y : 0xFFFFFFFFu);
+    const float wv = key_f32(kmax);
+    if (n >= k) {
+      const float last = sel_val[n - 1];
+      if (!(last - wv <= thr)) break;  // certified gap: the selection is closed
+    }
+    if (lane == 0) {
+      sel_idx[n] = (int)win;
+      sel_val[n] = wv;
+    }
+    if (head.x == kmax && head.y == win) {  // advance this list
+      ++pos;
+      head = pos < len ? lists[lane * L + pos] : make_uint2(0u, 0x7FFFFFFFu);
+    }
+    __syncwarp();
+    ++n;
+  }
+  __syncwarp();
+  resolve_runs(sel_idx, sel_val, n, k, thr, xt, router_w, prior, H, cache, scratch);
+}
+
 // Renormalised softmax weight of selected expert `lane` (lanes < k), i.e.
 // exp(l_j - m) / sum_i exp(l_i - m) over the k selected logits.
 static __device__ __forceinline__ float renormalised_weight(const float* sel_val, int k) {
   const int lane = threadIdx.x & 31;
-  float mx = -INFINITY;
-  for (int j = 0; j < k; ++j) mx = fmaxf(mx, sel_val[j]);
+  // any m that keeps exp(l - m) finite gives the same weights; the first
+  // selected logit is within rounding of the largest
+  const float mx = sel_val[0];
   const float ej = (lane < k) ? __expf(sel_val[lane] - mx) : 0.f;
   const float den = warp_sum(ej);
   return ej / den;
