@@ -191,9 +191,49 @@ static __device__ bool exact_before(const uint16_t* xt, const uint16_t* router_w
   return c > 0 || (c == 0 && a < b);
 }
 
-// Bytes of per-warp shared memory topk_select_warp needs for E experts.
+// Bytes of per-warp shared memory topk_select_warp needs for E experts:
+// sel_idx, sel_val, the exact-value cache, scratch, and the run members'
+// refined values, bounds and cache flags.
 __host__ __device__ constexpr size_t topk_warp_smem(int E) {
-  return (size_t)E * 8 + (size_t)(kRunCache + 2) * kDigits * 4;
+  return (size_t)E * 8 + (size_t)(kRunCache + 2) * kDigits * 4 + (size_t)kRunCache * 12;
+}
+
+// A tight fp32 logit of one router row, by one warp.  Lane l takes the
+// 8-element chunks c = l + 32 j of the row (8 sequential FMAs from zero per
+// chunk, chunk sums added in order), then a 5-level butterfly, then the
+// prior: depth D = 8 + H/256 + 6.  sum |x w| is computed alongside with the
+// same structure; 1 + 2^-8 covers its own rounding, so
+// bound = 2 D u (mag (1 + 2^-8) + |prior|) bounds the error (Higham, Accuracy
+// and Stability of Numerical Algorithms, Thm. 4.3).
+static __device__ void tight_logit_warp(const uint16_t* __restrict__ x,
+                                        const uint16_t* __restrict__ w, int H,
+                                        const float* prior_e, float& logit, float& bnd) {
+  const int lane = threadIdx.x & 31;
+  float acc = 0.f, mag = 0.f;
+  for (int j = 0; j < H / 256; ++j) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + lane + 32 * j);
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w) + lane + 32 * j);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    float sc = 0.f, mc = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float x0 = bf16_lo(xw[q]), x1 = bf16_hi(xw[q]);
+      const float w0 = bf16_lo(ww[q]), w1 = bf16_hi(ww[q]);
+      sc = fmaf(x0, w0, sc);
+      mc = fmaf(fabsf(x0), fabsf(w0), mc);
+      sc = fmaf(x1, w1, sc);
+      mc = fmaf(fabsf(x1), fabsf(w1), mc);
+    }
+    acc += sc;
+    mag += mc;
+  }
+  acc = warp_sum(acc);
+  mag = warp_sum(mag);
+  const float p = prior_e ? *prior_e : 0.f;
+  logit = acc + p;
+  const float depth = (float)(8 + H / 256 + 6);
+  bnd = 2.0f * depth * 5.9604644775390625e-8f * (mag * 1.00390625f + fabsf(p)) + kBoundFloor;
 }
 
 // Per-lane sort of (key, id) pairs, best first: larger key, then lower id.
@@ -343,13 +383,29 @@ __device__ int extract_sorted(uint32_t (&key)[N], int (&id)[N], int k, int limit
 }
 
 // Reorder, by exact values, every run of neighbours of sel[0..n) closer than
-// thr that reaches into the first k positions (one warp).  cache/scratch:
-// kRunCache*kDigits and 2*kDigits words of this warp's shared memory.
+// thr that reaches into the first k positions (one warp).  The run's members
+// are first recomputed with tight fp32 bounds (tight_logit_warp); two
+// members whose tight intervals are disjoint are ordered by them, and only
+// overlapping ones are compared exactly (values cached on first use).
+// cache/scratch: kRunCache*kDigits and 2*kDigits words; tl/tb/have:
+// kRunCache entries each (all this warp's shared memory).
 static __device__ void resolve_runs(int* sel_idx, float* sel_val, int n, int k, float thr,
                                     const uint16_t* xt, const uint16_t* router_w,
                                     const float* prior, int H, uint32_t* cache,
                                     uint32_t* scratch) {
   const int lane = threadIdx.x & 31;
+  float* tl = reinterpret_cast<float*>(scratch + 2 * kDigits);
+  float* tb = tl + kRunCache;
+  int* have = reinterpret_cast<int*>(tb + kRunCache);
+  auto ensure_exact = [&](int a0, int q) {
+    if (!have[q]) {
+      const int e = sel_idx[a0 + q];
+      exact_logit_warp(xt, router_w + (size_t)e * H, H, prior ? prior + e : nullptr, scratch);
+      if (lane < kDigits) cache[q * kDigits + lane] = scratch[lane];
+      if (lane == 0) have[q] = 1;
+      __syncwarp();
+    }
+  };
   int a = 0;
   while (a < n - 1 && a < k) {
     int b = a;
@@ -360,20 +416,46 @@ static __device__ void resolve_runs(int* sel_idx, float* sel_val, int n, int k, 
       if (m <= kRunCache) {
         for (int q = 0; q < m; ++q) {
           const int e = sel_idx[a + q];
-          exact_logit_warp(xt, router_w + (size_t)e * H, H, prior ? prior + e : nullptr,
-                           scratch);
-          if (lane < kDigits) cache[q * kDigits + lane] = scratch[lane];
-          __syncwarp();
+          float l, bb;
+          tight_logit_warp(xt, router_w + (size_t)e * H, H, prior ? prior + e : nullptr, l, bb);
+          if (lane == 0) {
+            tl[q] = l;
+            tb[q] = bb;
+            have[q] = 0;
+          }
         }
+        __syncwarp();
         // selection sort of the first `need` positions by (exact desc, id asc)
         for (int p = 0; p < need; ++p) {
           int best = p;
           for (int q = p + 1; q < m; ++q) {
-            const int c = exact_cmp(cache + q * kDigits, cache + best * kDigits);
+            int c;
+            if (tl[q] - tb[q] > tl[best] + tb[best]) {
+              c = 1;
+            } else if (tl[best] - tb[best] > tl[q] + tb[q]) {
+              c = -1;
+            } else {
+              ensure_exact(a, q);
+              ensure_exact(a, best);
+              c = exact_cmp(cache + q * kDigits, cache + best * kDigits);
+            }
             if (c > 0 || (c == 0 && sel_idx[a + q] < sel_idx[a + best])) best = q;
           }
           __syncwarp();
-          if (best != p) swap_sel(sel_idx, sel_val, cache, a, p, best);
+          if (best != p) {
+            swap_sel(sel_idx, sel_val, cache, a, p, best);
+            if (lane == 0) {
+              const float t0 = tl[p], t1 = tb[p];
+              const int h0 = have[p];
+              tl[p] = tl[best];
+              tb[p] = tb[best];
+              have[p] = have[best];
+              tl[best] = t0;
+              tb[best] = t1;
+              have[best] = h0;
+            }
+            __syncwarp();
+          }
         }
       } else {
         for (int p = 0; p < need; ++p) {
