@@ -13,6 +13,7 @@ namespace moe {
 namespace {
 
 constexpr int kPairsPerBlock = 2048;
+constexpr int kScatterWarps = 8;  // warps that scatter one block's pairs
 
 // Exclusive scan of one value per thread over a CTA of up to 1024 threads.
 __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
@@ -67,12 +68,52 @@ __device__ void warp_stable_scatter(const int32_t* __restrict__ topk_idx, int p0
   }
 }
 
+// Stable placement of pairs [p0, p1) by the first kScatterWarps warps of the
+// CTA: warp w takes a contiguous segment, counts it per expert into hist[w],
+// the counts become per-warp start positions (base[e] + the counts of the
+// earlier segments), and each warp places its segment in order.  Every thread
+// of the CTA calls (the barriers span the CTA).  hist: kScatterWarps * E ints
+// of shared memory.
+__device__ void block_stable_scatter(const int32_t* __restrict__ topk_idx, int p0, int p1,
+                                     const int* base, int E, int* hist,
+                                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                     int32_t* perm_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = ((p1 - p0 + kScatterWarps * 32 - 1) / (kScatterWarps * 32)) * 32;
+  const int w0 = min(p1, p0 + warp * seg), w1 = min(p1, w0 + seg);
+  int* h = hist + (size_t)warp * E;
+  if (warp < kScatterWarps)
+    for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncthreads();
+  if (warp < kScatterWarps) {
+    for (int b = w0; b < w1; b += 32) {
+      const int p = b + lane;
+      const int e = p < w1 ? topk_idx[p] : -1;
+      const unsigned mask = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == 31 - __clz(mask)) h[e] += __popc(mask);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = base[e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int t = hist[(size_t)w * E + e];
+      hist[(size_t)w * E + e] = run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  if (warp < kScatterWarps) warp_stable_scatter(topk_idx, w0, w1, h, perm, inv, perm_out);
+}
+
 // One CTA does everything (used when the pairs fit one block).
 __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t* __restrict__ topk_idx, int P, int E, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ used,
     int32_t* __restrict__ n_used, int32_t* perm_out, int32_t* offsets_out) {
   __shared__ int cnt[kMaxE];
+  __shared__ int hist[kScatterWarps * kMaxE];
   __shared__ int warp_tot[32];
   __shared__ int total, total_used;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -95,7 +136,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     *n_used = total_used;
   }
   __syncthreads();
-  if (threadIdx.x < 32) warp_stable_scatter(topk_idx, 0, P, cnt, perm, inv, perm_out);
+  block_stable_scatter(topk_idx, 0, P, cnt, E, hist, perm, inv, perm_out);
 }
 
 // Large P, pass 1: per-block expert counts.
@@ -141,15 +182,14 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(
   }
 }
 
-// Large P, pass 3: stable scatter of each block's pairs by one warp.
-__global__ void __launch_bounds__(32) permute_scatter_kernel(
+// Large P, pass 3: stable scatter of each block's pairs by kScatterWarps warps.
+__global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(
     const int32_t* __restrict__ topk_idx, int P, int E, const int32_t* __restrict__ hist,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* perm_out) {
-  __shared__ int pos[kMaxE];
-  for (int e = threadIdx.x; e < E; e += 32) pos[e] = hist[(size_t)blockIdx.x * E + e];
-  __syncwarp();
+  __shared__ int sh[kScatterWarps * kMaxE];
   const int p0 = blockIdx.x * kPairsPerBlock, p1 = min(P, p0 + kPairsPerBlock);
-  warp_stable_scatter(topk_idx, p0, p1, pos, perm, inv, perm_out);
+  block_stable_scatter(topk_idx, p0, p1, hist + (size_t)blockIdx.x * E, E, sh, perm, inv,
+                       perm_out);
 }
 
 }  // namespace
@@ -167,8 +207,8 @@ cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int*
   permute_count_kernel<<<nblk, 256, 0, st>>>(a.topk_idx, P, E, c.ws.hist);
   permute_scan_kernel<<<1, 1024, 0, st>>>(c.ws.hist, nblk, E, c.ws.offsets, c.ws.used,
                                            c.ws.n_used, a.offsets_out);
-  permute_scatter_kernel<<<nblk, 32, 0, st>>>(a.topk_idx, P, E, c.ws.hist, c.ws.perm, c.ws.inv,
-                                               a.perm_out);
+  permute_scatter_kernel<<<nblk, kScatterWarps * 32, 0, st>>>(a.topk_idx, P, E, c.ws.hist,
+                                                                c.ws.perm, c.ws.inv, a.perm_out);
   *launches += 3;
   return cudaGetLastError();
 }
