@@ -127,6 +127,14 @@ cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& a, cudaStream_t st,
 cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
 
+// Router for many tokens: approximate logits on the tensor cores, then
+// certified logits of each token's candidates and the exact selection.
+bool router_tc_supported(const Dims& d, int T);
+cudaError_t prepare_router_tc();
+cudaError_t launch_router_tc(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_router_candidates(const Ctx& c, const FwdArgs& a, cudaStream_t st,
+                                     int* launches);
+
 cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);

@@ -185,25 +185,43 @@ __global__ void __launch_bounds__(256, 2) router_tile_kernel(
 #pragma unroll
     for (int j = 0; j < 4; ++j) tot[i][j] = make_float2(0.f, 0.f);
   const int kbeg = blockIdx.z * cps * kTK, kend = min(H, kbeg + cps * kTK);
+  // the next chunk's words of this thread, loaded while the current one is
+  // multiplied (x: 2 of the 512 16-byte words, Wr: 4 of the 1024)
+  static_assert(kTT * kTK / 8 == 2 * 256 && kTE * kTK / 8 == 4 * 256, "staging split");
+  uint4 px[2], pw[4];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = tid + 256 * r, tt = i % kTT, hc = i / kTT;
+      px[r] = t0 + tt < T
+                  ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0) + hc)
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tid + 256 * r, ee = i % kTE, hc = i / kTE;
+      pw[r] = e0 + ee < E ? __ldg(reinterpret_cast<const uint4*>(router_w + (size_t)(e0 + ee) * H +
+                                                                  k0) + hc)
+                          : make_uint4(0, 0, 0, 0);
+    }
+  };
+  fetch(kbeg);
   for (int k0 = kbeg; k0 < kend; k0 += kTK) {
-    __syncthreads();
-    for (int i = tid; i < kTT * kTK / 8; i += 256) {
-      const int tt = i % kTT, hc = i / kTT;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t0 + tt < T) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0) + hc);
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    __syncthreads();  // the previous chunk's products are done
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = tid + 256 * r, tt = i % kTT, hc = i / kTT;
+      const uint32_t vw[4] = {px[r].x, px[r].y, px[r].z, px[r].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         xs[hc * 8 + 2 * q][tt] = bf16_lo(vw[q]);
         xs[hc * 8 + 2 * q + 1][tt] = bf16_hi(vw[q]);
       }
     }
-    for (int i = tid; i < kTE * kTK / 8; i += 256) {
-      const int ee = i % kTE, hc = i / kTE;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (e0 + ee < E)
-        v = __ldg(reinterpret_cast<const uint4*>(router_w + (size_t)(e0 + ee) * H + k0) + hc);
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tid + 256 * r, ee = i % kTE, hc = i / kTE;
+      const uint32_t vw[4] = {pw[r].x, pw[r].y, pw[r].z, pw[r].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         ws[hc * 8 + 2 * q][ee] = bf16_lo(vw[q]);
@@ -211,6 +229,7 @@ __global__ void __launch_bounds__(256, 2) router_tile_kernel(
       }
     }
     __syncthreads();
+    if (k0 + kTK < kend) fetch(k0 + kTK);
     float2 acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -356,6 +375,10 @@ cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* 
     router_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a.x, a.T, c.router_w, c.d.E,
                                                        c.shared_gate_w, c.d.H, c.ws.xnorm,
                                                        c.ws.wnorm, c.ws.gate_z);
+    if (router_tc_supported(c.d, a.T)) {
+      ++*launches;
+      return launch_router_tc(c, a, st, launches);
+    }
     const int tiles = ((a.T + kTT - 1) / kTT) * ((c.d.E + kTE - 1) / kTE);
     const int chunks = c.d.H / kTK;
     // slices of H so that about two CTAs per SM are busy (one slice when the tiles suffice)
@@ -383,11 +406,14 @@ cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* 
 
 cudaError_t prepare_router(const Ctx& c) {
   cudaError_t e = set_router_smem_limit(c.d.H);
-  if (e != cudaSuccess) return e;
-  return set_topk_smem_limits();
+  if (e == cudaSuccess) e = set_topk_smem_limits();
+  if (e == cudaSuccess) e = prepare_router_tc();
+  return e;
 }
 
 cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches) {
+  if (a.T >= kTileRouterMinT && router_tc_supported(c.d, a.T))
+    return launch_router_candidates(c, a, st, launches);
   ++*launches;
   return launch_topk_any(c.ws.logits, c.ws.bound, c.ws.gate_z, a.x, c.router_w, c.router_bias,
                          a.T, c.d.E, c.d.H, c.d.k, a.topk_idx, a.topk_w, c.ws.gate, st);

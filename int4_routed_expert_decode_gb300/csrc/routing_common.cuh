@@ -482,10 +482,13 @@ struct PlainLogits {
     logit = __ldcg(l + e);
     bnd = __ldcg(b + e);
   }
+  __device__ __forceinline__ int id(int e) const { return e; }
 };
 
 // The k experts of one token in exact order, by one warp.
-//   src: the token's E fp32 logits and their bounds (src.get(e, logit, bound))
+//   src: the token's E fp32 logits and their bounds (src.get(i, logit, bound))
+//        and the expert id of entry i (src.id(i); entries may be a subset of
+//        the experts in any order)
 //   xt: the token's bf16 x (global); router_w, prior: router weights and prior
 //   smem: topk_warp_smem(E) bytes of this warp's shared memory
 // On return sel_idx[0..k) / sel_val[0..k) (inside smem) hold the experts in
@@ -520,7 +523,7 @@ __device__ void topk_select_warp_src(const Src& src, int E, int k, const uint16_
     if (e < E) src.get(e, l, bnd);
     if (l != l) l = -INFINITY;  // a NaN logit from bad input ranks as -inf
     key[i] = (e < E) ? f32_key(l) : 0u;  // key 0: empty (below every real logit)
-    id[i] = (e < E) ? e : 0x7FFFFFFF;
+    id[i] = (e < E) ? src.id(e) : 0x7FFFFFFF;
     if (e < E) bmax = max(bmax, __float_as_uint(bnd));
   }
   const float thr = 2.0f * __uint_as_float(__reduce_max_sync(0xffffffffu, bmax));
@@ -571,7 +574,7 @@ __device__ void topk_select_block(const Src& src, int E, int k, const uint16_t* 
     if (e < E) src.get(e, l, bnd);
     if (l != l) l = -INFINITY;
     key[v] = (e < E) ? f32_key(l) : 0u;
-    id[v] = (e < E) ? e : 0x7FFFFFFF;
+    id[v] = (e < E) ? src.id(e) : 0x7FFFFFFF;
     if (e < E) bm = max(bm, __float_as_uint(bnd));
   }
   bm = __reduce_max_sync(0xffffffffu, bm);

@@ -202,6 +202,16 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ---- TMA (tensor maps live in kernel parameter space; x coordinates are
 // element indices along the innermost dimension, 16-byte aligned)
+// 2-D tile copy global -> shared, completion on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 3-D tile copy global -> shared, completion on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2,
                                             uint64_t* bar) {

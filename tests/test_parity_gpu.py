@@ -535,3 +535,38 @@ def test_prefill_path_graph_replay():
         assert L.status() == moe.MOE_OK
         assert np.array_equal(idx.cpu().numpy(), ref["topk_idx"])
         U.assert_y_close(U.to_f64_bf16(y), ref["y"], what="prefill graph")
+
+
+# ------------------------------------------------------------------ tensor-core router (T >= 128)
+TC_SHAPE = synth.Shape(E=256, k=8, H=512, I=128, Is=128, G=64)
+
+
+def test_tc_router_parity_with_prior():
+    """Approximate logits on the tensor cores, certified candidates, exact order."""
+    W = synth.layer_weights(0, 0, 21, TC_SHAPE, zipf_s=0.8)
+    x = synth.tokens(0, 0, 21, 0, 300, TC_SHAPE.H)
+    L = U.layer(TC_SHAPE, W, max_T=300)
+    ref = O.moe_block(x, W, TC_SHAPE.k, TC_SHAPE.G)
+    U.assert_parity(U.run(L, x), ref, what="tc router")
+
+
+def test_tc_router_duplicate_rows_tie_exactly():
+    """Thirty identical router rows: their logits tie exactly; lower ids first."""
+    W = synth.layer_weights(0, 0, 22, TC_SHAPE)
+    rw = W["router_w"]
+    rw[40:70] = rw[5]
+    x = synth.tokens(0, 0, 22, 0, 130, TC_SHAPE.H)
+    L = U.layer(TC_SHAPE, W, max_T=130)
+    ref = O.moe_block(x, W, TC_SHAPE.k, TC_SHAPE.G)
+    U.assert_parity(U.run(L, x), ref, what="tc router ties")
+
+
+def test_tc_router_all_rows_equal():
+    """Every expert is a candidate and every logit ties: experts 0..k-1."""
+    W = synth.layer_weights(0, 0, 23, TC_SHAPE)
+    W["router_w"] = np.repeat(W["router_w"][:1], TC_SHAPE.E, axis=0)
+    x = synth.tokens(0, 0, 23, 0, 128, TC_SHAPE.H)
+    L = U.layer(TC_SHAPE, W, max_T=128)
+    out = U.run(L, x)
+    assert out["topk_idx"].tolist() == [list(range(TC_SHAPE.k))] * 128
+    U.assert_parity(out, O.moe_block(x, W, TC_SHAPE.k, TC_SHAPE.G), what="tc router all equal")
