@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--path", type=int, default=0, help="kernel path (0 auto)")
+    p.add_argument("--profile", action="store_true",
+                   help="short run for profilers: no clock-warming loop, no end-to-end or "
+                        "stage timing, no CPU baseline")
     return p.parse_args()
 
 
@@ -72,6 +75,37 @@ def peaks():
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "source": "fallback"}
+
+
+# DRAM bytes per launch of the dominant kernels, from ncu captures
+# (profiles/traffic.json), with the hash of the sources they were taken on:
+# reported only while those sources are unchanged.
+TRAFFIC_SOURCES = {
+    "fused_decode_kernel": ["fused_decode.cu", "routing_common.cuh", "device_util.cuh",
+                            "sm100_ptx.cuh", "moe_internal.cuh"],
+    "grouped_gemm_kernel<gate/up>": ["prefill.cu", "device_util.cuh", "sm100_ptx.cuh",
+                                     "moe_internal.cuh"],
+}
+
+
+def sources_sha256(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "int4_routed_expert_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel, workload):
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    if t.get("workload") != workload or t.get("sources_sha256") != sources_sha256(kernel):
+        return None
+    return t.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -318,7 +352,7 @@ def run_ours(args, wl):
         # keep the GPU loaded ~1 s so that clock samples exist before timing
         t_load = time.perf_counter()
         i = 0
-        while time.perf_counter() - t_load < 1.0:
+        while not args.profile and time.perf_counter() - t_load < 1.0:
             graphs[i % S].replay()
             i += 1
             if i % 64 == 0:
@@ -339,8 +373,9 @@ def run_ours(args, wl):
         ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     # per-stage device times of layer 0 (eager, same stream, after the timed region)
-    stages = stage_times(moe, torch, layers[0].ctx, enqueue, [x_all[s] for s in range(S)],
-                         stream, k=max(3, min(args.steps, 20)))
+    stages = {} if args.profile else stage_times(
+        moe, torch, layers[0].ctx, enqueue, [x_all[s] for s in range(S)], stream,
+        k=max(3, min(args.steps, 20)))
     t_max = ms
     if world > 1:
         tt = torch.tensor([ms], device="cuda")
@@ -357,7 +392,7 @@ def run_ours(args, wl):
     x_host = torch.empty((L, T, H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x_all[0].cpu())
     y_host = torch.empty((L, T, H), dtype=torch.bfloat16, pin_memory=True)
-    k_e2e = max(1, min(args.steps, 200))
+    k_e2e = 1 if args.profile else max(1, min(args.steps, 200))
     with torch.cuda.stream(stream):
         for _ in range(3):
             x_in.copy_(x_host, non_blocking=True)
@@ -378,7 +413,7 @@ def run_ours(args, wl):
     # CPU oracle on the host cores (rank 0, N = 1), and a parity spot check
     cpu = None
     parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         v, n, dt, sample, results = oracle_units(wl, args.cpu_budget, L)
         cpu = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                "sample": sample + f", {dt:.1f} s"}
@@ -397,12 +432,13 @@ def run_ours(args, wl):
              "down": 2.0 * H * (wl.I * P + wl.Is * T), "router": 2.0 * H * wl.E * T}
     flops_layer = sum(flops.values())
     grouped = args.path == 3 or (args.path == 0 and T > 1)  # tensor-core grouped GEMMs
-    if grouped:
+    if grouped and "gateup" in stages:
         # many tokens: the grouped GEMMs are tensor-core bound; the gate/up GEMM dominates
         t_gu = stages["gateup"] * 1e-6
         achieved = flops["gateup"] / t_gu / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                    "traffic": measured_traffic("grouped_gemm_kernel<gate/up>", wl.name),
                     "kernel": "grouped_gemm_kernel<gate/up> (tcgen05 bf16, fp32 TMEM), "
                               f"{flops['gateup'] / 1e9:.1f} GFLOP algorithmic per launch, "
                               f"{stages['gateup']:.1f} us per launch",
@@ -411,7 +447,9 @@ def run_ours(args, wl):
         algo_bytes_layer = unique_per_step / L + wl.router_bytes + 2 * T * H * 2
         achieved = algo_bytes_layer / (us_layer * 1e-6) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                    "frac": achieved / pk["hbm_gbs"],
+                    "traffic": measured_traffic("fused_decode_kernel", wl.name)
+                    if launches_per_layer == 1 else None,
                     "kernel": f"one layer of moe_forward ({launches_per_layer} launches), "
                               f"{algo_bytes_layer / 1e6:.2f} MB algorithmic per layer",
                     "peak_source": pk["source"]}
