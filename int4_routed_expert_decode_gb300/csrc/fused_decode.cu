@@ -156,20 +156,6 @@ __device__ __forceinline__ float load_chunk_bf16(const uint16_t* src, float2 (&v
   return s;
 }
 
-// 32 consecutive fp32 written earlier in this kernel (read through L2).
-__device__ __forceinline__ float load_chunk_f32(const float* src, float2 (&v)[16]) {
-  const float4* p = reinterpret_cast<const float4*>(src);
-  float s = 0.f;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 u = __ldcg(p + q);
-    v[2 * q] = make_float2(u.x, u.y);
-    v[2 * q + 1] = make_float2(u.z, u.w);
-    s += (u.x + u.y) + (u.z + u.w);
-  }
-  return s;
-}
-
 // A 16-byte aligned window [lo, hi) around bytes [b0, b1) of a region whose
 // size is a multiple of 16: returns lo and the padded length.
 __device__ __forceinline__ void align16(uint64_t b0, uint64_t b1, uint64_t& lo, uint32_t& len) {
@@ -410,52 +396,86 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   grid_barrier(a.bar, nC + a.bar_extra, a.err);
 
   // ---------------------------------------------------------------- P4
-  // A group of `lpu` lanes owns one expert j (j == k: the shared one); lane
-  // `sub` holds chunk `sub` of h_j in registers and walks this CTA's rows.
-  // The trip counts depend on the warp only, so the group sums see every lane.
-  wait_or_flag(&mbar[kNumMbar - 1], 0, a.err);
+  // h of the selected experts and of the shared one into shared memory (the
+  // P3 rows are dead now; 16-byte piece q of 32-float chunk c is stored at
+  // piece q ^ (c & 7), so that the 16 lanes of a group reading chunks c..c+15
+  // hit distinct banks), with each chunk's sum.  Then 16-lane groups take this
+  // CTA's (expert, row) pairs round robin: every warp works, and a group's
+  // serial chain is ~(k+1) nrow / 16 rows instead of nrow.
   {
-    int lpu = 1;
-    while (lpu * 2 <= 32 && lpu * 2 <= IC) lpu *= 2;
-    const int upw = 32 / lpu, sub = lane % lpu;
-    const int ngroups = kWarps * upw;
-    for (int jb = warp * upw; jb <= k; jb += ngroups) {
-      const int j = jb + lane / lpu;
-      const bool in_range = j <= k;
-      const bool shared = in_range && j == k;
-      const bool valid = in_range && (shared || s_slot[j] >= 0) && sub < IC;
-      float2 hr[16];
-      float hsum = 0.f;
-      if (valid)
-        hsum = load_chunk_f32((shared ? a.hs : a.h + (size_t)j * I) + sub * 32, hr);
-      const uint8_t* qbase =
-          shared ? sd_q : sm + a.sm.p4 + (size_t)(in_range ? j : 0) * a.sm.p4_expert;
-      const uint8_t* sbbase = shared ? sd_sb + dsb_off
-                                     : sm + a.sm.p4 + (size_t)(in_range ? j : 0) * a.sm.p4_expert +
-                                           a.sm.p4_sb + dsb_off;
-      // four rows at a time: their chunk terms and group sums are independent
-      for (int rb = 0; rb < nrow; rb += 4) {
-        float v[4];
+    float4* s_h4 = reinterpret_cast<float4*>(sm + a.sm.p3);
+    const int n4 = k * I / 4, ns4 = I / 4;
+    for (int i = threadIdx.x; i < n4 + ns4; i += kThreads) {
+      const float4 v = i < n4 ? __ldcg(reinterpret_cast<const float4*>(a.h) + i)
+                              : __ldcg(reinterpret_cast<const float4*>(a.hs) + (i - n4));
+      const int hc = i >> 3;
+      s_h4[(hc << 3) | ((i ^ hc) & 7)] = v;
+    }
+  }
+  wait_or_flag(&mbar[kNumMbar - 1], 0, a.err);
+  __syncthreads();
+  {
+    const float4* s_h4 = reinterpret_cast<const float4*>(sm + a.sm.p3);
+    float* s_x = reinterpret_cast<float*>(sm + a.sm.p3) + (size_t)(k + 1) * I;  // chunk sums
+    for (int hc = threadIdx.x; hc < (k + 1) * IC; hc += kThreads) {
+      float sum = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int rl = rb + u;
-          v[u] = 0.f;
-          if (valid && rl < nrow) {
-            const uint4 q = reinterpret_cast<const uint4*>(qbase + (size_t)rl * (I / 2))[sub];
-            const uint32_t sbw =
-                reinterpret_cast<const uint32_t*>(sbbase + (size_t)rl * IG * 4)[sub * 32 / G];
-            v[u] = chunk_term(q, sbw, hr, hsum);
+      for (int q = 0; q < 8; ++q) {
+        const float4 u = s_h4[hc * 8 + ((q + hc) & 7)];  // rotated: distinct banks
+        sum += (u.x + u.y) + (u.z + u.w);
+      }
+      s_x[hc] = sum;
+    }
+    __syncthreads();
+    constexpr int kG = 16;                // lanes per pair
+    constexpr int kGroups = kThreads / kG;
+    const int grp = threadIdx.x / kG, sub = lane % kG;
+    const int npairs = (k + 1) * nrow;
+    // two pairs per group and pass (their shuffle reductions overlap); the
+    // trip count depends on the warp only, so every shuffle sees all lanes
+    for (int pb = 0; pb + 2 * warp < npairs; pb += 2 * kGroups) {
+      float v[2];
+      int jj[2], rr[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pp = pb + u * kGroups + grp;
+        v[u] = 0.f;
+        jj[u] = -1;
+        rr[u] = 0;
+        if (pp < npairs) {
+          const int j = pp / nrow, rl = pp - j * nrow;
+          const bool shared = j == k;
+          if (shared || s_slot[j] >= 0) {
+            jj[u] = j;
+            rr[u] = rl;
+            const uint8_t* eb = sm + a.sm.p4 + (size_t)j * a.sm.p4_expert;
+            const uint4* qrow =
+                reinterpret_cast<const uint4*>((shared ? sd_q : eb) + (size_t)rl * (I / 2));
+            const uint32_t* sbrow = reinterpret_cast<const uint32_t*>(
+                (shared ? sd_sb : eb + a.sm.p4_sb) + dsb_off + (size_t)rl * IG * 4);
+            for (int ch = sub; ch < IC; ch += kG) {
+              const int hc = j * IC + ch;
+              float2 hr[16];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 t = s_h4[hc * 8 + (q ^ (hc & 7))];
+                hr[2 * q] = make_float2(t.x, t.y);
+                hr[2 * q + 1] = make_float2(t.z, t.w);
+              }
+              v[u] += chunk_term(qrow[ch], sbrow[ch * 32 / G], hr, s_x[hc]);
+            }
           }
         }
-        for (int o = lpu >> 1; o > 0; o >>= 1) {
+      }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], o);
-        }
-        if (in_range && sub == 0) {
+      for (int o = kG >> 1; o > 0; o >>= 1) {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        v[1] += __shfl_xor_sync(0xffffffffu, v[1], o);
+      }
+      if (sub == 0) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (rb + u < nrow) ypart[(rb + u) * (k + 1) + j] = v[u];
-        }
+        for (int u = 0; u < 2; ++u)
+          if (jj[u] >= 0) ypart[rr[u] * (k + 1) + jj[u]] = v[u];
       }
     }
   }
@@ -504,7 +524,8 @@ bool plan_smem(const Ctx& c, int nC, FusedSmem& s) {
   const uint32_t per_cta = (uint32_t)((R + nC - 1) / nC);
   s.seg_max = (per_cta + kWarps - 1) / kWarps;
   s.p3_warp = up(s.seg_max * (H + 8 * (H / G)), 128);
-  s.p3 = take(kWarps * s.p3_warp);
+  const uint32_t h_bytes = (uint32_t)(k + 1) * (I + I / 32) * 4;  // P4: h and chunk sums
+  s.p3 = take(kWarps * s.p3_warp > h_bytes ? kWarps * s.p3_warp : h_bytes);
   s.p4_sb = up(s.nrow_max * (I / 2), 16);
   s.p4_expert = up(s.p4_sb + dsb_max, 128);
   s.p4 = take(s.p4_expert * k);

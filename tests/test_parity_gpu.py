@@ -282,9 +282,12 @@ def test_fused_decode_agrees_with_general_path(wid):
 
 
 def test_fused_decode_other_shapes():
-    """Group 128, hidden 1024, E = 64 (list length 8), larger k."""
+    """Group 128, hidden 1024, E = 64 (list length 8), larger k; inter 192 and 768,
+    whose 32-code chunk counts (6, 24) are not powers of two."""
     for shape in (synth.Shape(E=64, k=6, H=1024, I=256, Is=256, G=128),
-                  synth.Shape(E=300, k=12, H=512, I=128, Is=128, G=32)):
+                  synth.Shape(E=300, k=12, H=512, I=128, Is=128, G=32),
+                  synth.Shape(E=32, k=4, H=512, I=192, Is=192, G=64),
+                  synth.Shape(E=16, k=3, H=256, I=768, Is=768, G=64)):
         W = synth.layer_weights(0, 0, 21, shape, zipf_s=0.5)
         L = U.layer(shape, W, max_T=1)
         moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
