@@ -64,6 +64,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest replica's time: the whole job ends when the last rank does."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(t_max_ms, world, tokens, layers, steps):
+    """Layer-tokens per second of the whole job: every replica runs the same steps."""
+    return world * tokens * layers * steps / (t_max_ms / 1e3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -376,13 +392,8 @@ def run_ours(args, wl):
     stages = {} if args.profile else stage_times(
         moe, torch, layers[0].ctx, enqueue, [x_all[s] for s in range(S)], stream,
         k=max(3, min(args.steps, 20)))
-    t_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
-    sec = t_max / 1e3
-    value = world * T * L * args.steps / sec
+    t_max = max_over_ranks(ms, world, "cuda")
+    value = job_throughput(t_max, world, T, L, args.steps)
     ms_step = t_max / args.steps
     us_layer = ms_step * 1e3 / L
     hbm = unique_per_step / (ms_step / 1e3) / 1e9
