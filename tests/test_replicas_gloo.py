@@ -29,7 +29,7 @@ def _rank_main(rank, world, port, times, out):
 
 def test_max_over_ranks_and_job_throughput_gloo():
     world, times = 2, [80.0, 125.0]
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a threaded process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), times, out), nprocs=world, join=True)
         res = dict(out)
