@@ -80,8 +80,11 @@ struct FusedArgs {
   FusedSmem sm;
 };
 
+// Start of share p of n items split into `parts` shares.  n * p < 2^32 for
+// every split here (n <= 32768 row pairs, p <= the SM count), so 32-bit
+// arithmetic suffices and avoids a 64-bit division routine at every use.
 __device__ __forceinline__ int part(int n, int parts, int p) {
-  return (int)(((long long)n * p) / parts);
+  return (int)(((uint32_t)n * (uint32_t)p) / (uint32_t)parts);
 }
 
 // Grid-wide barrier on a monotonic 64-bit arrival counter: barrier number b
