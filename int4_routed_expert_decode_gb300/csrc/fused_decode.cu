@@ -77,14 +77,23 @@ struct FusedArgs {
   uint32_t bar_extra;  // test hook: arrivals the barrier waits for beyond the grid
   int32_t* err;
   int E, k, I, G;
+  uint64_t inv_nc, inv_i;  // ceil(2^32 / gridDim.x), ceil(2^32 / I): see udiv
   FusedSmem sm;
 };
 
-// Start of share p of n items split into `parts` shares.  n * p < 2^32 for
-// every split here (n <= 32768 row pairs, p <= the SM count), so 32-bit
-// arithmetic suffices and avoids a 64-bit division routine at every use.
-__device__ __forceinline__ int part(int n, int parts, int p) {
-  return (int)(((uint32_t)n * (uint32_t)p) / (uint32_t)parts);
+// x / d for x * d < 2^32, with m = ceil(2^32 / d) from the host: writing
+// m d = 2^32 + e (0 <= e < d), x m / 2^32 = x / d + x e / (d 2^32) and the
+// excess is below 1/d, so the floor is exact.  Two instructions instead of a
+// division routine; this code runs once per launch, where every instruction
+// counts.
+__device__ __forceinline__ int udiv(uint32_t x, uint64_t m) {
+  return (int)(((uint64_t)x * m) >> 32);
+}
+
+// Start of share p of n items split into gridDim.x shares (n * p * gridDim.x
+// < 2^32 here: n <= 32768 row pairs, p <= gridDim.x <= a few hundred).
+__device__ __forceinline__ int part(int n, int p, uint64_t inv_nc) {
+  return udiv((uint32_t)n * (uint32_t)p, inv_nc);
 }
 
 // Grid-wide barrier on a monotonic 64-bit arrival counter: barrier number b
@@ -186,11 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
 
   // unit ranges of this CTA
   const int U1 = E + I + 1;  // router rows, shared features, gate vector
-  const int u0 = part(U1, nC, c), u1 = part(U1, nC, c + 1);
+  const int u0 = part(U1, c, a.inv_nc), u1 = part(U1, c + 1, a.inv_nc);
   const int re0 = min(u0, E), re1 = min(u1, E);
   const int si0 = min(max(u0 - E, 0), I), si1 = min(max(u1 - E, 0), I);
   const bool has_gv = (u0 <= E + I) && (E + I < u1);
-  const int r0 = part(H, nC, c), r1 = part(H, nC, c + 1), nrow = r1 - r0;
+  const int r0 = part(H, c, a.inv_nc), r1 = part(H, c + 1, a.inv_nc), nrow = r1 - r0;
 
   uint8_t* p1_rw = sm + a.sm.p1;
   uint8_t* p1_gq = p1_rw + (size_t)(re1 - re0) * H * 2;
@@ -317,22 +326,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   // P3 / P4 copies: each warp its own gate/up segment; the last warp also
   // fetches this CTA's rows of every selected expert's down projection
   const int R = k * I;
-  const int R0 = part(R, nC, c), R1 = part(R, nC, c + 1);
+  const int R0 = part(R, c, a.inv_nc), R1 = part(R, c + 1, a.inv_nc);
   const int seg = (R1 - R0 + kWarps - 1) / kWarps;
   const int w0 = min(R1, R0 + warp * seg), w1 = min(R1, w0 + seg);
   uint8_t* p3w = sm + a.sm.p3 + (size_t)warp * a.sm.p3_warp;
   uint8_t* p3w_sb = p3w + (size_t)a.sm.seg_max * H;
   const uint32_t rp_sb = 8 * HG;  // sb bytes of one row-pair
+  const int jw0 = udiv((uint32_t)w0, a.inv_i);  // expert of the segment's first row pair
   if (lane == 0) {
     uint32_t bytes = 0;
-    for (int r = w0; r < w1;) {
-      const int j = r / I, n = min(w1, (j + 1) * I) - r;
+    for (int j = jw0, r = w0; r < w1; ++j) {
+      const int n = min(w1, (j + 1) * I) - r;
       if (s_slot[j] >= 0) bytes += (uint32_t)n * (H + rp_sb);
       r += n;
     }
     ptx::mbar_arrive_expect_tx(&mbar[1 + warp], bytes);
-    for (int r = w0; r < w1;) {
-      const int j = r / I, i = r % I, n = min(w1, (j + 1) * I) - r;
+    for (int j = jw0, r = w0; r < w1; ++j) {
+      const int i = r - j * I, n = min(w1, (j + 1) * I) - r;
       if (s_slot[j] >= 0) {
         const uint8_t* blob = a.pool + (uint64_t)s_slot[j] * a.L.stride;
         ptx::bulk_g2s(p3w + (size_t)(r - w0) * H, blob + a.L.gu_q + (size_t)i * H,
@@ -363,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   }
   // outputs of the permutation (T = 1: pair p = j)
   if (a.offsets_out) {
-    for (int e = part(E + 1, nC, c) + threadIdx.x; e < part(E + 1, nC, c + 1); e += kThreads) {
+    for (int e = part(E + 1, c, a.inv_nc) + threadIdx.x; e < part(E + 1, c + 1, a.inv_nc);
+         e += kThreads) {
       int cnt = 0;
       for (int j = 0; j < k; ++j) cnt += s_idx[j] < e;
       a.offsets_out[e] = cnt;
@@ -377,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
 
   // ---------------------------------------------------------------- P3
   wait_or_flag(&mbar[1 + warp], 0, a.err);
-  for (int r = w0; r < w1; ++r) {
-    const int j = r / I, i = r % I;
+  for (int r = w0, j = jw0, i = w0 - jw0 * I; r < w1; ++r, i = (i + 1 == I) ? 0 : i + 1,
+           j += (i == 0)) {
     if (s_slot[j] < 0) continue;
     const uint4* q4 = reinterpret_cast<const uint4*>(p3w + (size_t)(r - w0) * H);
     const uint32_t* sb = reinterpret_cast<const uint32_t*>(p3w_sb + (size_t)(r - w0) * rp_sb);
@@ -648,6 +659,8 @@ cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& fa, cudaStream_t st
   a.I = d.I;
   a.G = d.G;
   const int nC = c.fused_ctas;
+  a.inv_nc = ((1ull << 32) + (uint64_t)nC - 1) / (uint64_t)nC;
+  a.inv_i = ((1ull << 32) + (uint64_t)d.I - 1) / (uint64_t)d.I;
   if (!plan_smem(c, nC, a.sm)) return cudaErrorInvalidConfiguration;
   ++*launches;
   return dispatch<LaunchF>(d, (const FusedArgs*)&a, nC, st);
