@@ -78,6 +78,7 @@ struct FusedArgs {
   int32_t* err;
   int E, k, I, G;
   uint64_t inv_nc, inv_i;  // ceil(2^32 / gridDim.x), ceil(2^32 / I): see udiv
+  uint64_t inv_nrow[2];    // the same for the two row counts H / gridDim.x (+1) of P4
   FusedSmem sm;
 };
 
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
         jj[u] = -1;
         rr[u] = 0;
         if (pp < npairs) {
-          const int j = pp / nrow, rl = pp - j * nrow;
+          const int j = udiv((uint32_t)pp, a.inv_nrow[nrow == a.sm.nrow_max]), rl = pp - j * nrow;
           const bool shared = j == k;
           if (shared || s_slot[j] >= 0) {
             jj[u] = j;
@@ -661,6 +662,9 @@ cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& fa, cudaStream_t st
   const int nC = c.fused_ctas;
   a.inv_nc = ((1ull << 32) + (uint64_t)nC - 1) / (uint64_t)nC;
   a.inv_i = ((1ull << 32) + (uint64_t)d.I - 1) / (uint64_t)d.I;
+  const uint64_t nr_lo = (uint64_t)(d.H / nC), nr_hi = (uint64_t)((d.H + nC - 1) / nC);
+  a.inv_nrow[0] = nr_lo ? ((1ull << 32) + nr_lo - 1) / nr_lo : 0;
+  a.inv_nrow[1] = ((1ull << 32) + nr_hi - 1) / nr_hi;
   if (!plan_smem(c, nC, a.sm)) return cudaErrorInvalidConfiguration;
   ++*launches;
   return dispatch<LaunchF>(d, (const FusedArgs*)&a, nC, st);
