@@ -79,6 +79,7 @@ struct FusedArgs {
   int E, k, I, G;
   uint64_t inv_nc, inv_i;  // ceil(2^32 / gridDim.x), ceil(2^32 / I): see udiv
   uint64_t inv_nrow[2];    // the same for the two row counts H / gridDim.x (+1) of P4
+  uint64_t inv_bar;        // ceil(2^64 / barrier arrivals): see grid_barrier
   FusedSmem sm;
 };
 
@@ -99,14 +100,17 @@ __device__ __forceinline__ int part(int n, int p, uint64_t inv_nc) {
 
 // Grid-wide barrier on a monotonic 64-bit arrival counter: barrier number b
 // (counting from the last reset) is passed once the counter reaches
-// (b + 1) * n, so one atomic round trip per CTA suffices.  Polls stop after
-// kBarSpin tries or one second; on expiry the sticky error word gets
-// MOE_ERR_TIMEOUT and the CTA carries on (no trap, no hang).
-__device__ void grid_barrier(unsigned long long* bar, uint32_t n, int32_t* err) {
+// (b + 1) * n, so one atomic round trip per CTA suffices, and the last
+// arrival's atomic is itself the release.  b = old / n comes from a
+// multiply-high with inv_n = ceil(2^64 / n) (exact while old < 2^64 / n; see
+// udiv) instead of a 64-bit division routine.  Polls stop after kBarSpin
+// tries or one second; on expiry the sticky error word gets MOE_ERR_TIMEOUT
+// and the CTA carries on (no trap, no hang).
+__device__ void grid_barrier(unsigned long long* bar, uint32_t n, uint64_t inv_n, int32_t* err) {
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned long long old = ptx::atom_add_acq_rel_u64(bar, 1ull);
-    const unsigned long long target = (old / n + 1) * n;
+    const unsigned long long target = (__umul64hi(old, inv_n) + 1) * n;
     if (old + 1 < target) {
       const uint64_t t0 = ptx::globaltimer_ns();
       uint32_t it = 0;
@@ -186,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nC = gridDim.x, c = blockIdx.x;
   const int E = a.E, k = a.k, I = a.I, G = a.G;
-  const int HG = H / G, IG = I / G, IC = I / 32;
+  const int lg = 31 - __clz(G);  // G is 32, 64 or 128: shifts instead of divisions
+  const int HG = H >> lg, IG = I >> lg, IC = I / 32;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.sm.mbar);
   int* s_idx = reinterpret_cast<int*>(sm + a.sm.misc);
   float* s_w = reinterpret_cast<float*>(sm + a.sm.misc + 128);
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       for (int m = 0; m < MC; ++m) {
         const int ch = lane + 32 * m;
         if (ch < HC) {
-          const int g = ch * 32 / G;
+          const int g = (ch * 32) >> lg;
           ag += chunk_term(q4[ch], sb[g], xr[m], xs_r[m]);
           au += chunk_term(q4[HC + ch], sb[HG + g], xr[m], xs_r[m]);
         }
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
       if (lane == 0) a.hs[i] = silu_f(ag) * au;
     }
   }
-  grid_barrier(a.bar, nC + a.bar_extra, a.err);
+  grid_barrier(a.bar, nC + a.bar_extra, a.inv_bar, a.err);
 
   // ---------------------------------------------------------------- P2
   {
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
     for (int m = 0; m < MC; ++m) {
       const int ch = lane + 32 * m;
       if (ch < HC) {
-        const int g = ch * 32 / G;
+        const int g = (ch * 32) >> lg;
         ag += chunk_term(q4[ch], sb[g], xr[m], xs_r[m]);
         au += chunk_term(q4[HC + ch], sb[HG + g], xr[m], xs_r[m]);
       }
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
     au = warp_sum(au);
     if (lane == 0) a.h[(size_t)j * I + i] = silu_f(ag) * au;
   }
-  grid_barrier(a.bar, nC + a.bar_extra, a.err);
+  grid_barrier(a.bar, nC + a.bar_extra, a.inv_bar, a.err);
 
   // ---------------------------------------------------------------- P4
   // h of the selected experts and of the shared one into shared memory (the
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
                 hr[2 * q] = make_float2(t.x, t.y);
                 hr[2 * q + 1] = make_float2(t.z, t.w);
               }
-              v[u] += chunk_term(qrow[ch], sbrow[ch * 32 / G], hr, s_x[hc]);
+              v[u] += chunk_term(qrow[ch], sbrow[(ch * 32) >> lg], hr, s_x[hc]);
             }
           }
         }
@@ -665,6 +670,10 @@ cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& fa, cudaStream_t st
   const uint64_t nr_lo = (uint64_t)(d.H / nC), nr_hi = (uint64_t)((d.H + nC - 1) / nC);
   a.inv_nrow[0] = nr_lo ? ((1ull << 32) + nr_lo - 1) / nr_lo : 0;
   a.inv_nrow[1] = ((1ull << 32) + nr_hi - 1) / nr_hi;
+  {
+    const uint64_t nb = (uint64_t)nC + a.bar_extra;  // ceil(2^64 / nb) = floor((2^64 - 1) / nb) + 1
+    a.inv_bar = ~0ull / nb + 1;
+  }
   if (!plan_smem(c, nC, a.sm)) return cudaErrorInvalidConfiguration;
   ++*launches;
   return dispatch<LaunchF>(d, (const FusedArgs*)&a, nC, st);
