@@ -41,7 +41,7 @@ using namespace rt;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
-constexpr uint32_t kBarSpin = 1u << 22;    // grid-barrier polls (with sleeps and a 1 s limit)
+constexpr uint32_t kBarSpin = 1u << 22;    // grid-barrier polls (and a 1 s limit)
 constexpr uint32_t kMbarTries = 1u << 22;  // mbarrier try_waits
 constexpr int kNumMbar = 10;               // 0: P0 weights, 1..8: P3 warps, 9: P4 down rows
 
@@ -104,8 +104,9 @@ __device__ __forceinline__ int part(int n, int p, uint64_t inv_nc) {
 // arrival's atomic is itself the release.  b = old / n comes from a
 // multiply-high with inv_n = ceil(2^64 / n) (exact while old < 2^64 / n; see
 // udiv) instead of a 64-bit division routine.  Polls stop after kBarSpin
-// tries or one second; on expiry the sticky error word gets MOE_ERR_TIMEOUT
-// and the CTA carries on (no trap, no hang).
+// tries or one second (no sleep between polls: each is an L2 round trip,
+// and a sleep would only delay the wake-up); on expiry the sticky error word
+// gets MOE_ERR_TIMEOUT and the CTA carries on (no trap, no hang).
 __device__ void grid_barrier(unsigned long long* bar, uint32_t n, uint64_t inv_n, int32_t* err) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -119,7 +120,6 @@ __device__ void grid_barrier(unsigned long long* bar, uint32_t n, uint64_t inv_n
           record_error(err, MOE_ERR_TIMEOUT);
           break;
         }
-        __nanosleep(32);
       }
     }
   }
