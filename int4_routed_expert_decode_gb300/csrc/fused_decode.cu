@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_decode_kernel(const FusedAr
     topk_select_block<MAXV / kWarps>(PlainLogits{a.logits, a.bound}, E, k, a.x, a.router_w,
                                      a.prior, H, sm + a.sm.topk,
                                      reinterpret_cast<uint2*>(sm + a.sm.lists),
-                                     reinterpret_cast<float*>(sm + a.sm.lists + (size_t)E * 8),
+                                     reinterpret_cast<float*>(sm + a.sm.lists + MAXV * 32 * 8),
                                      &sel_idx, &sel_val);
     if (warp == 0) {
       const float w = renormalised_weight(sel_val, k);
@@ -523,7 +523,9 @@ bool plan_smem(const Ctx& c, int nC, FusedSmem& s) {
   s.mbar = take(kNumMbar * 8);
   s.misc = take(512);
   s.topk = take((uint32_t)topk_warp_smem(E));
-  s.lists = take((uint32_t)E * 8 + kWarps * 4);
+  // every warp's whole list (32 V entries, padding included), then the bounds
+  const int mv = E <= 256 ? 8 : E <= 512 ? 16 : 32;  // MAXV of the dispatch
+  s.lists = take((uint32_t)mv * 32 * 8 + kWarps * 4);
   // P1: worst CTA of router rows * 2H + shared features * (H + 8H/G)
   const int U1 = E + I + 1;
   uint32_t p1 = 0;

@@ -265,55 +265,6 @@ __device__ __forceinline__ void sort_lane_desc(uint32_t (&key)[N], int (&id)[N])
   }
 }
 
-// Bitonic sort across a warp of N = 32 V (key, id) pairs, best first (larger
-// key, then lower id; key 0 = empty sorts last).  Entry i = lane * V + v.
-// Stages with distance >= V exchange through shuffles, shorter ones stay in
-// registers (Batcher's bitonic network).
-template <int V>
-__device__ __forceinline__ void warp_bitonic_sort(uint32_t (&key)[V], int (&id)[V]) {
-  const int lane = threadIdx.x & 31;
-  constexpr int N = 32 * V;
-#pragma unroll
-  for (int kk = 2; kk <= N; kk <<= 1) {
-#pragma unroll
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      if (j >= V) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const int i = lane * V + v;
-          const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[v], j / V);
-          const int pid = __shfl_xor_sync(0xffffffffu, id[v], j / V);
-          const bool p_better = pk > key[v] || (pk == key[v] && pid < id[v]);
-          const bool lower = (i & j) == 0, up = (i & kk) == 0;
-          // in an "up" block the lower index keeps the better entry
-          if ((lower == up) ? p_better : !p_better && (pk != key[v] || pid != id[v])) {
-            key[v] = pk;
-            id[v] = pid;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          const int p = v ^ j;
-          if (p > v) {
-            const int i = lane * V + v;
-            const bool up = (i & kk) == 0;
-            const bool p_better = key[p] > key[v] || (key[p] == key[v] && id[p] < id[v]);
-            if (up ? p_better : !p_better) {
-              const uint32_t tk = key[v];
-              key[v] = key[p];
-              key[p] = tk;
-              const int ti = id[v];
-              id[v] = id[p];
-              id[p] = ti;
-            }
-          }
-        }
-      }
-    }
-  }
-}
-
 // Swap entries p and q of the selection (and of the exact-value cache when
 // `cache` is given); one warp, positions relative to `base`.
 static __device__ __forceinline__ void swap_sel(int* sel_idx, float* sel_val, uint32_t* cache,
@@ -543,14 +494,15 @@ __device__ void topk_select_warp(const float* lrow, const float* brow, int E, in
 }
 
 // The same selection by all `nw` warps of a CTA (E <= nw * 32 * V), for
-// latency: warp w sorts experts [32 V w, 32 V (w + 1)) across its lanes
+// latency: warp w rank-sorts experts [32 V w, 32 V (w + 1)) across its lanes
 // (best first; ties to the lower id) into `lists` (shared memory, E entries
 // of (key, id)), then warp 0 merges the nw lists -- lane l < nw holds the
 // head of list l -- with the closing rule and the run resolution of
 // topk_select_warp_src, so the result is identical.  Every thread of the CTA
 // calls; the selection is complete on return (one __syncthreads inside, none
 // after: sel_idx / sel_val are written by warp 0).
-//   smem: topk_warp_smem(E) bytes; lists: E * 8 bytes; bmx: nw floats.
+//   smem: topk_warp_smem(E) bytes; lists: nw * 32 V entries of 8 bytes (whole
+//   lists: the padding past E is written too); bmx: nw floats after them.
 template <int V, typename Src>
 __device__ void topk_select_block(const Src& src, int E, int k, const uint16_t* xt,
                                   const uint16_t* router_w, const float* prior, int H,
@@ -574,14 +526,37 @@ __device__ void topk_select_block(const Src& src, int E, int k, const uint16_t* 
     if (e < E) src.get(e, l, bnd);
     if (l != l) l = -INFINITY;
     key[v] = (e < E) ? f32_key(l) : 0u;
-    id[v] = (e < E) ? src.id(e) : 0x7FFFFFFF;
+    id[v] = (e < E) ? src.id(e) : e;  // padding: key 0 (never taken), a distinct id
     if (e < E) bm = max(bm, __float_as_uint(bnd));
   }
   bm = __reduce_max_sync(0xffffffffu, bm);
-  warp_bitonic_sort<V>(key, id);
   if (warp * L < E) {
+    // rank sort of the warp's list: an entry's position is the number of
+    // entries before it (larger key, or equal key and lower id), counted
+    // against 64-bit keys read back from shared memory as broadcasts --
+    // independent compares instead of a network of dependent shuffles
+    uint64_t ck[V];
+    uint64_t* cks = reinterpret_cast<uint64_t*>(lists + warp * L);
 #pragma unroll
-    for (int v = 0; v < V; ++v) lists[warp * L + lane * V + v] = make_uint2(key[v], (uint32_t)id[v]);
+    for (int v = 0; v < V; ++v) {
+      ck[v] = ((uint64_t)key[v] << 32) | (uint32_t)~(uint32_t)id[v];
+      cks[lane * V + v] = ck[v];
+    }
+    __syncwarp();
+    int rank[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) rank[v] = 0;
+    const uint4* kp = reinterpret_cast<const uint4*>(cks);
+#pragma unroll 4
+    for (int u = 0; u < L / 2; ++u) {
+      const uint4 w = kp[u];
+      const uint64_t a0 = ((uint64_t)w.y << 32) | w.x, a1 = ((uint64_t)w.w << 32) | w.z;
+#pragma unroll
+      for (int v = 0; v < V; ++v) rank[v] += (int)(a0 > ck[v]) + (int)(a1 > ck[v]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int v = 0; v < V; ++v) lists[warp * L + rank[v]] = make_uint2(key[v], (uint32_t)id[v]);
   }
   if (lane == 0) bmx[warp] = __uint_as_float(bm);
   __syncthreads();
