@@ -316,6 +316,32 @@ def test_fused_decode_ties_and_near_ties():
     assert out["topk_idx"].tolist() == [list(range(W0.k))]
 
 
+def test_fused_decode_near_ties_across_partial_lists():
+    """E = 300: the block top-k's last warp list is partial (entries 256..299 of
+    256..319).  Near-tied experts spread over several warp lists, the partial one
+    included, are lifted into the top-k by a prior, so their order rests on the
+    bounds that every warp stores next to the lists."""
+    shape = synth.Shape(E=300, k=12, H=512, I=128, Is=128, G=32)
+    W = synth.layer_weights(0, 0, 25, shape)
+    rw = W["router_w"].copy()
+    tied = [5, 70, 140, 200, 260, 277, 299]
+    for j, e in enumerate(tied):
+        rw[e] = rw[tied[0]]
+        if j % 2:
+            rw[e, (7 * j) % shape.H] ^= 1  # one bf16 ulp at a different column
+    W["router_w"] = rw
+    bias = np.zeros(shape.E, np.float32)
+    bias[tied] = 8.0
+    W["router_bias"] = bias
+    L = U.layer(shape, W, max_T=1)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+    for step in range(4):
+        x = synth.tokens(0, 0, 25, step, 1, shape.H)
+        out = U.run(L, x)
+        assert set(tied) <= set(out["topk_idx"][0].tolist())
+        U.assert_parity(out, O.moe_block(x, W, shape.k, shape.G), what=f"partial lists step{step}")
+
+
 def test_fused_decode_placement_invariance():
     wl = synth.WORKLOADS[1]
     W = _weights(wl, layer=2)
