@@ -90,11 +90,12 @@ typedef struct moe_weights {
 } moe_weights;
 
 /* Create a context for one MoE layer.
- *   E in [1, 1024]; k in [1, min(E, 32)]; hidden a multiple of 256, at most
- *   8192; inter and shared_inter multiples of group, at most 4096; group in
- *   {32, 64, 128}.  Nothing is allocated on the device yet.
- * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for sizes out of range,
- * MOE_ERR_CUDA if no device is current. */
+ *   E in [1, 1024]; k in [1, min(E, 32)]; hidden in {256, 512, 1024, 2048,
+ *   4096, 8192}; inter and shared_inter multiples of group, at most 4096;
+ *   group in {32, 64, 128}.  Nothing is allocated on the device yet.
+ * Errors: MOE_ERR_INVALID_ARG for k or a NULL `out`; MOE_ERR_UNSUPPORTED for
+ * E, hidden, inter, shared_inter or group outside those sets; MOE_ERR_CUDA if
+ * no device is current. */
 int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out);
 
 /* Copy and repack the weights into library-owned device memory: the routed
@@ -221,10 +222,12 @@ int moe_last_launch_count(const moe_ctx* ctx);
  *   topk_idx       int32 [T][k] device, written (same contract as moe_forward)
  *   topk_w         fp32 [T][k] device, written
  *   shared_gate    fp32 [T] device, written: sigmoid(x_t . shared_gate_w)
- * Sizes: E in [1, 1024], k in [1, min(E, 32)], hidden a multiple of 256 up to
- * 8192, T in [0, MOE_STATIC_ROUTE_MAX_T] and T*E <= MOE_STATIC_ROUTE_MAX_LOGITS;
- * larger sizes return MOE_ERR_INVALID_ARG with a message for
- * moe_last_error(NULL).
+ * Sizes: E in [1, 1024], k in [1, min(E, 32)], hidden in {256, 512, 1024,
+ * 2048, 4096, 8192}, T in [0, MOE_STATIC_ROUTE_MAX_T] and
+ * T*E <= MOE_STATIC_ROUTE_MAX_LOGITS.  A hidden outside that set returns
+ * MOE_ERR_UNSUPPORTED; every other size out of range returns
+ * MOE_ERR_INVALID_ARG; both leave a message for moe_last_error(NULL) and
+ * launch nothing.
  * Scratch: the intermediates live in one file-scope device array of
  * (2 * MOE_STATIC_ROUTE_MAX_LOGITS + MOE_STATIC_ROUTE_MAX_T) floats (1 MiB +
  * 16 KiB), held by every device that loads the library until the process

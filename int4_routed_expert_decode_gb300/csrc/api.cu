@@ -181,9 +181,9 @@ int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group,
     return set_msg(nullptr, MOE_ERR_INVALID_ARG, "k=%d not in [1, min(E, %d)]", k, kMaxK);
   if (group != 32 && group != 64 && group != 128)
     return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "group=%d not in {32, 64, 128}", group);
-  if (hidden < 256 || hidden > kMaxH || hidden % 256 != 0)
-    return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "hidden=%d must be a multiple of 256 in [256, %d]",
-                   hidden, kMaxH);
+  if (!hidden_supported(hidden))
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED,
+                   "hidden=%d not in {256, 512, 1024, 2048, 4096, 8192}", hidden);
   if (inter < group || inter > kMaxInter || inter % group != 0 || shared_inter < group ||
       shared_inter > kMaxInter || shared_inter % group != 0)
     return set_msg(nullptr, MOE_ERR_UNSUPPORTED,

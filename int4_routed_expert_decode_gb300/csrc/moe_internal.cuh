@@ -13,6 +13,10 @@ constexpr int kMaxK = 32;
 constexpr int kMaxH = 8192;
 constexpr int kMaxInter = 4096;
 constexpr int kSyncWords = 1;  // counters of the fused decode kernel
+// hidden sizes the router kernels are instantiated for: 256 * 2^j up to kMaxH
+inline bool hidden_supported(int H) {
+  return H >= 256 && H <= kMaxH && H % 256 == 0 && ((H / 256) & (H / 256 - 1)) == 0;
+}
 constexpr int kTileRouterMinT = 16;  // from this many tokens the router is a tiled GEMM
 // Floats of the router's slice sums: the slices are only used while
 // slices x tiles <= 2 x SMs, and a tile covers 64 x 128 logits.

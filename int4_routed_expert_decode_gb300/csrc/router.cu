@@ -486,9 +486,9 @@ extern "C" int moe_route_static(const void* x, int T, const uint16_t* router_w,
     snprintf(msg, sizeof msg, "moe_route_static: E=%d, k=%d out of range", E, k);
     return set_global_msg(MOE_ERR_INVALID_ARG, msg);
   }
-  if (hidden < 256 || hidden > kMaxH || hidden % 256 != 0) {
-    snprintf(msg, sizeof msg, "moe_route_static: hidden=%d must be a multiple of 256 in [256, %d]",
-             hidden, kMaxH);
+  if (!hidden_supported(hidden)) {
+    snprintf(msg, sizeof msg, "moe_route_static: hidden=%d not in {256, 512, 1024, 2048, 4096, 8192}",
+             hidden);
     return set_global_msg(MOE_ERR_UNSUPPORTED, msg);
   }
   if ((int64_t)T * E > kStaticMaxLogits) {

@@ -43,6 +43,8 @@ def test_status_strings(L):
     ((0, 1, 256, 64, 64, 32), moe.MOE_ERR_UNSUPPORTED),     # E = 0
     ((16, 17, 256, 64, 64, 32), moe.MOE_ERR_INVALID_ARG),   # k > E
     ((16, 2, 300, 64, 64, 32), moe.MOE_ERR_UNSUPPORTED),    # hidden not a multiple of 256
+    ((16, 2, 768, 64, 64, 32), moe.MOE_ERR_UNSUPPORTED),    # hidden / 256 not a power of two
+    ((16, 2, 3072, 64, 64, 32), moe.MOE_ERR_UNSUPPORTED),   # the same
     ((16, 2, 256, 64, 64, 48), moe.MOE_ERR_UNSUPPORTED),    # group
     ((16, 2, 256, 80, 64, 32), moe.MOE_ERR_UNSUPPORTED),    # inter not a multiple of group
     ((2048, 8, 2048, 512, 512, 64), moe.MOE_ERR_UNSUPPORTED),  # E too large
@@ -67,3 +69,12 @@ def test_null_context_is_an_error_not_a_crash(L):
 def test_python_binding_names_match_c(L):
     for n in moe.EXPORTS:
         assert callable(getattr(moe, n)), n
+
+
+@pytest.mark.parametrize("hidden", [768, 1280, 1536, 3072])
+def test_static_routing_rejects_uninstantiated_hidden_up_front(L, hidden):
+    """hidden sizes that no router kernel is built for are refused before any
+    device call, with MOE_ERR_UNSUPPORTED (nothing is launched)."""
+    rc = L.moe_route_static(None, 1, None, None, None, 16, 2, hidden, None, None, None, None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    assert "hidden" in moe.moe_last_error(None)

@@ -48,8 +48,11 @@ def test_static_routing_matches_moe_forward_on_two_calls(wid, T):
         assert layer.status() == moe.MOE_OK
         assert torch.equal(idx, idx_ref), f"call {step}: topk_idx differs from moe_forward"
         assert torch.max(torch.abs(w - w_ref)).item() <= U.W_ABS, f"call {step}: topk_w"
-        ref_gate = O.sigmoid(O.bf16_to_f64(x_np) @ O.bf16_to_f64(W["shared_gate_w"]))
-        assert np.max(np.abs(g.cpu().numpy() - ref_gate)) <= 1e-5, f"call {step}: shared gate"
+        # and directly against the CPU oracle's routing of the same tokens
+        o_idx, o_w, o_gate, _ = O.route(x_np, W, wl.k)
+        assert np.array_equal(idx.cpu().numpy(), o_idx), f"call {step}: topk_idx vs oracle"
+        assert np.max(np.abs(w.cpu().numpy() - o_w)) <= U.W_ABS, f"call {step}: topk_w vs oracle"
+        assert np.max(np.abs(g.cpu().numpy() - o_gate)) <= 1e-5, f"call {step}: shared gate"
     layer.close()
 
 
