@@ -67,6 +67,33 @@ void free_workspace(Ctx& c) {
   c.ws = Workspace{};
   c.err = nullptr;
   c.max_T = 0;
+  c.dec_layer = nullptr;
+  c.dec_ws = DecWorkspace{};
+  c.dec_ok = 0;
+}
+
+// The descriptor the persistent decode kernel reads for this layer (written
+// once the weights and the workspace both exist).
+cudaError_t refresh_decode_layer(Ctx& c) {
+  if (!c.pool || !c.dec_layer) return cudaSuccess;
+  DecLayer D{};
+  D.router_w = c.router_w;
+  D.prior = c.router_bias;
+  D.shared_gate_w = c.shared_gate_w;
+  D.norm_w = nullptr;
+  D.pool = c.pool;
+  D.shared_blob = c.shared;
+  D.wmax = c.dec_wmax;
+  D.pmax = c.dec_pmax;
+  D.stride = c.ex.stride;
+  D.gu_q = c.ex.gu_q;
+  D.gu_sb = c.ex.gu_sb;
+  D.d_q = c.ex.d_q;
+  D.d_sb = c.ex.d_sb;
+  D.n_slots = c.n_slots;
+  if (c.dec_ok && !decode_encode_maps(c.d, c.pool, c.ex, c.n_slots, c.shared, c.sh, &D))
+    return cudaErrorInvalidValue;
+  return cudaMemcpy(c.dec_layer, &D, sizeof D, cudaMemcpyHostToDevice);
 }
 
 uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
@@ -242,6 +269,18 @@ int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stre
   }
   int rc = load_experts(ctx, w->gate, w->up, w->down, 0, n_slots, w->on_device, d.H, d.I, d.G,
                         c.pool, c.ex, st);
+  if (rc == MOE_OK) {  // the decode kernel's bound constants, kept on the host
+    float* tmp = nullptr;
+    float hv[2] = {0.f, 0.f};
+    e = cudaMalloc(&tmp, 2 * sizeof(float));
+    if (e == cudaSuccess) e = decode_router_consts(c.router_w, c.router_bias, d.E, d.H, tmp, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hv, tmp, sizeof hv, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) rc = cuda_fail(ctx, e, "router bound constants");
+    c.dec_wmax = hv[0];
+    c.dec_pmax = hv[1];
+  }
   if (rc == MOE_OK)
     rc = load_experts(ctx, w->shared_gate, w->shared_up, w->shared_down, 0, 1, w->on_device, d.H,
                       d.Is, d.G, c.shared, c.sh, st);
@@ -251,6 +290,7 @@ int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stre
     return rc;
   }
   c.n_slots = n_slots;
+  if ((e = refresh_decode_layer(c)) != cudaSuccess) return cuda_fail(ctx, e, "decode descriptor");
   c.weight_bytes = (int64_t)rw_bytes + d.H * 2 + (w->router_bias ? d.E * 4 : 0) +
                    (int64_t)n_slots * c.ex.stride + (int64_t)c.sh.stride;
   return MOE_OK;
@@ -297,6 +337,8 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_bar = take(kSyncWords * 8);
   const uint64_t o_tiles = take((uint64_t)prefill_max_tiles(d, max_T) * 16);
   const uint64_t o_ntiles = take(4);
+  const uint64_t o_dlayer = take(sizeof(DecLayer));
+  const uint64_t o_dws = take(decode_workspace_bytes(d, n_sms));
   uint8_t* base = nullptr;
   cudaError_t e = cudaMalloc(&base, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace alloc");
@@ -326,6 +368,12 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.bar = (unsigned long long*)(base + o_bar);
   c.ws.tiles = base + o_tiles;
   c.ws.n_tiles = (int32_t*)(base + o_ntiles);
+  c.dec_layer = (DecLayer*)(base + o_dlayer);
+#ifdef MOE_DECODE_STAMPS
+  cudaMalloc(&c.dec_stamps, (size_t)n_sms * 16 * 8);
+  cudaMemset(c.dec_stamps, 0, (size_t)n_sms * 16 * 8);
+#endif
+  decode_workspace_carve(d, n_sms, base + o_dws, &c.dec_ws);
   c.max_T = max_T;
   if ((e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, c.device)) !=
       cudaSuccess) {
@@ -334,6 +382,8 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   }
   if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess ||
       (e = prepare_fused_decode(c)) != cudaSuccess ||
+      (e = decode_prepare(d, c.num_sms, false, &c.dec_ok)) != cudaSuccess ||
+      (e = refresh_decode_layer(c)) != cudaSuccess ||
       (prefill_supported(d) && (e = prepare_prefill(c)) != cudaSuccess)) {
     free_workspace(c);
     return cuda_fail(ctx, e, "kernel attributes");
@@ -366,7 +416,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   cudaStream_t st = (cudaStream_t)stream;
   FwdArgs a{(const uint16_t*)x, T, expert_slot_table, (uint16_t*)y, topk_idx, topk_w, perm, offsets};
   int launches = 0;
-  const bool fused_ok = T == 1 && fused_decode_supported(c);
+  const bool fused_ok = T == 1 && (c.dec_ok || fused_decode_supported(c));
   const bool prefill_ok = prefill_supported(c.d);
   if (c.path == MOE_PATH_DECODE && !fused_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
@@ -380,7 +430,28 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
       c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > 1);
   cudaError_t e;
   record_mark(c, MOE_MARK_START, st);
-  if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE)) {
+  if (fused_ok && c.dec_ok && c.path == MOE_PATH_DECODE) {
+    DecLaunch p{};
+    p.layers = c.dec_layer;
+    p.L = 1;
+    p.x = a.x;
+    p.y = a.y;
+    p.topk_idx = a.topk_idx;
+    p.topk_w = a.topk_w;
+    p.perm = a.perm_out;
+    p.offsets = a.offsets_out;
+    p.tables = a.table;
+    p.ws = c.dec_ws;
+    p.err = c.err;
+    p.timeout_hook = (c.test_flags & MOE_TEST_WAIT_TIMEOUT) != 0;
+    p.cooperative = c.cooperative;
+#ifdef MOE_DECODE_STAMPS
+    p.stamps = c.dec_stamps;
+#endif
+    ++launches;
+    e = decode_launch(c.d, c.num_sms, p, st);
+  } else if (fused_ok && (c.path == MOE_PATH_AUTO || c.path == MOE_PATH_DECODE ||
+                          c.path == kPathFusedV1)) {
     e = launch_fused_decode(c, a, st, &launches);
   } else {
     e = launch_router(c, a, st, &launches);
@@ -468,7 +539,7 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
 
 int moe_set_path(moe_ctx* ctx, int path) {
   if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_PREFILL)
+  if (path < MOE_PATH_AUTO || path > kPathFusedV1)
     return set_msg(ctx, MOE_ERR_INVALID_ARG, "path=%d unknown", path);
   ctx->c.path = path;
   return MOE_OK;
@@ -514,3 +585,19 @@ void moe_destroy(moe_ctx* ctx) {
 }
 
 }  // extern "C"
+
+#ifdef MOE_DECODE_STAMPS
+// Instrumented builds only: the per-CTA phase timestamps of the last decode
+// launch ([CTA][8] nanoseconds of %globaltimer) and the launch attribute knob.
+extern "C" int moe_debug_decode_stamps(moe_ctx* ctx, unsigned long long* host, int n) {
+  if (!ctx || !ctx->c.dec_stamps) return MOE_ERR_INVALID_ARG;
+  return cudaMemcpy(host, ctx->c.dec_stamps, (size_t)n * 8, cudaMemcpyDeviceToHost) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+extern "C" int moe_debug_set_cooperative(moe_ctx* ctx, int on) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  ctx->c.cooperative = on != 0;
+  return MOE_OK;
+}
+#endif

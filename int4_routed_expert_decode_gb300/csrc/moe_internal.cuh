@@ -1,6 +1,7 @@
 // moe_internal.cuh -- shared declarations of the CUDA library (host + device).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,7 +18,8 @@ constexpr int kSyncWords = 1;  // counters of the fused decode kernel
 inline bool hidden_supported(int H) {
   return H >= 256 && H <= kMaxH && H % 256 == 0 && ((H / 256) & (H / 256 - 1)) == 0;
 }
-constexpr int kTileRouterMinT = 16;  // from this many tokens the router is a tiled GEMM
+constexpr int kTileRouterMinT = 16;
+constexpr int kPathFusedV1 = 4;  // the earlier barrier-based fused decode kernel (comparison)  // from this many tokens the router is a tiled GEMM
 // Floats of the router's slice sums: the slices are only used while
 // slices x tiles <= 2 x SMs, and a tile covers 64 x 128 logits.
 inline int64_t tile_router_part_floats(int num_sms) { return (int64_t)2 * num_sms * 64 * 128; }
@@ -36,6 +38,43 @@ BlobLayout make_blob_layout(int H, int I, int G);
 
 struct Dims {
   int E, k, H, I, Is, G;
+};
+
+// cuTensorMapEncodeTiled, reached through the runtime (null if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
+
+// ---- persistent decode kernel (decode.cu): one token, one launch per layer
+// or per stack of layers chained through RMSNorm and a residual add.
+// Per-layer resident weights and constants, read by the kernel from device
+// memory (and copied into shared memory with each layer's prologue).
+struct alignas(64) DecLayer {
+  // TMA maps of the packed codes (rows of 128-byte column blocks, 128-byte
+  // swizzle where a row holds at least 128 bytes): routed gate/up
+  // {H/2 bytes, 2I rows, slots} box {128, 8, 1}; routed down {I/2, H, slots}
+  // box {min(128, I/2), 16, 1}; the shared expert's the same with one slot
+  CUtensorMap map_gu, map_d, map_sgu, map_sd;
+  const uint16_t* router_w;       // [E][H]
+  const float* prior;             // [E] or null
+  const uint16_t* shared_gate_w;  // [H]
+  const uint16_t* norm_w;         // [H] or null (stacks)
+  const uint8_t* pool;            // routed blobs
+  const uint8_t* shared_blob;     // the shared expert (same layout: inter == shared_inter)
+  uint64_t stride, gu_q, gu_sb, d_q, d_sb;
+  int n_slots;
+  float wmax, pmax;  // max_e |Wr_e|_2 and max_e |prior_e|, rounded up
+};
+// Exchange state of one decode launch sequence (zeroed once, never reset:
+// the counters only grow).
+struct DecWorkspace {
+  uint32_t* seq;             // [CTAs] launch counters
+  unsigned long long* cnt;   // logits, h and residual counters, 128 bytes apart
+  float* lt;                 // [E] logits
+  float* ht;                 // [(k + 1) I] SwiGLU activations (shared expert last)
+  uint16_t* xt;              // [H] residual (stacks)
 };
 
 // Workspace carved out of one allocation by moe_reserve.
@@ -82,6 +121,15 @@ struct Ctx {
   int32_t* err = nullptr;             // sticky device error word
   int num_sms = 0;                    // multiprocessors of the device
   int fused_ctas = 0;                 // CTAs of the fused decode kernel (0: unavailable)
+  float dec_wmax = 0.f, dec_pmax = 0.f;  // router bound constants (with the weights)
+  DecLayer* dec_layer = nullptr;      // this layer's descriptor (in the workspace)
+  DecWorkspace dec_ws{};              // decode exchange state (in the workspace)
+  int dec_ok = 0;                     // the persistent decode kernel fits these shapes
+  // Launch a single layer with the cooperative attribute?  Measured: it keeps
+  // the next launch from starting until this one has fully drained (about
+  // 2.5 us per layer), so single-layer launches go without it (stacks use it).
+  bool cooperative = false;
+  unsigned long long* dec_stamps = nullptr;  // phase timestamps (instrumented builds only)
   int test_flags = 0;                 // MOE_TEST_* hooks
   cudaEvent_t marks[MOE_MARK_COUNT] = {};  // borrowed stage events (moe_set_stage_events)
   int n_marks = 0;
@@ -120,6 +168,38 @@ cudaError_t prepare_general_experts(const Ctx& c);
 bool fused_decode_supported(const Ctx& c);
 cudaError_t prepare_fused_decode(Ctx& c);
 cudaError_t launch_fused_decode(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+
+// ---- persistent decode kernel (decode.cu), continued
+struct DecLaunch {
+  const DecLayer* layers;
+  int L;
+  const uint16_t* x;
+  uint16_t* x_out;
+  uint16_t* y;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* perm;
+  int32_t* offsets;
+  const int32_t* tables;
+  int chain;
+  float eps;
+  DecWorkspace ws;
+  int32_t* err;
+  int timeout_hook;
+  unsigned long long* stamps;
+  bool cooperative;
+};
+bool decode_shape_ok(const Dims& d);
+bool decode_fits(const Dims& d, int nC, bool chain);
+cudaError_t decode_prepare(const Dims& d, int nC, bool chain, int* ok);
+size_t decode_workspace_bytes(const Dims& d, int nC);
+void decode_workspace_carve(const Dims& d, int nC, uint8_t* base, DecWorkspace* w);
+cudaError_t decode_router_consts(const uint16_t* router_w, const float* prior, int E, int H,
+                                 float* out, cudaStream_t st);
+// The four TMA maps of a layer's descriptor (host-side encoding).
+bool decode_encode_maps(const Dims& d, const uint8_t* pool, const BlobLayout& ex, int n_slots,
+                        const uint8_t* shared, const BlobLayout& sh, DecLayer* D);
+cudaError_t decode_launch(const Dims& d, int nC, const DecLaunch& p, cudaStream_t st);
 
 // Tensor-core grouped GEMM path for many tokens: availability, workspace
 // size (tiles for max_T tokens), one-time set-up, launch (after router, top-k

@@ -666,15 +666,8 @@ cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& fa, cudaStream_t st
   return cudaMemsetAsync(c.ws.o, 0, (size_t)T * d.H * 4, st);
 }
 
-namespace {
-
 // cuTensorMapEncodeTiled through the runtime's driver entry point, so that
 // the library does not link the driver library (it loads without a GPU).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_tiled() {
   static EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
@@ -688,6 +681,8 @@ EncodeTiledFn encode_tiled() {
   }();
   return fn;
 }
+
+namespace {
 
 // Packed codes of `blobs` blobs: 3-D uint32 {K/8 words, rows, blobs}, box
 // 8 x 128 x 1 (the 64 codes of one K-chunk for 128 weight rows), no swizzle.

@@ -204,14 +204,16 @@ __host__ __device__ constexpr size_t topk_warp_smem(int E) {
 // prior: depth D = 8 + H/256 + 6.  sum |x w| is computed alongside with the
 // same structure; 1 + 2^-8 covers its own rounding, so
 // bound = 2 D u (mag (1 + 2^-8) + |prior|) bounds the error (Higham, Accuracy
-// and Stability of Numerical Algorithms, Thm. 4.3).
+// and Stability of Numerical Algorithms, Thm. 4.3).  x is a generic pointer
+// (global or shared memory); w is global.
 static __device__ void tight_logit_warp(const uint16_t* __restrict__ x,
                                         const uint16_t* __restrict__ w, int H,
                                         const float* prior_e, float& logit, float& bnd) {
   const int lane = threadIdx.x & 31;
   float acc = 0.f, mag = 0.f;
   for (int j = 0; j < H / 256; ++j) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + lane + 32 * j);
+    // x may live in shared memory (the decode kernel keeps its block input there)
+    const uint4 xv = reinterpret_cast<const uint4*>(x)[lane + 32 * j];
     const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w) + lane + 32 * j);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};

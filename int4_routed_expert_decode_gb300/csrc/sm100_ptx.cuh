@@ -256,6 +256,12 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long
   return old;
 }
 
+// Release-add without a return value (gpu scope): publishes every write that
+// happens before it, including other threads' writes ordered by a CTA barrier.
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // ---- nanosecond global timer
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
