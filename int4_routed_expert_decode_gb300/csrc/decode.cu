@@ -185,54 +185,65 @@ struct TileGeom {
   bool swz;
 };
 
-// One task of a 16-row tile: chunks [c0, c1) of K (32 inputs each, c0 and c1
-// even and whole groups), folded per group.  Thread (g = lane / 4, t = lane % 4)
-// ends with rows g and g + 8 of the tile in out0 / out1 when t == 0.
+// One task of a 16-row tile: chunks [c0, c1) of K (32 inputs each; c0 and c1
+// multiples of max(2, chunks per group)), folded per group of 2^LCPG chunks.
+// Thread (g = lane / 4, t = lane % 4) ends with rows g and g + 8 of the tile
+// in out0 / out1 when t == 0.
 //   tile   shared address of the tile
-//   bsrc   the permuted input (16 bytes per (chunk, t)) this thread supplies
-//          for its column g of N, or null for a zero column
+//   bcol   this thread's column of N: the permuted input (16 bytes per
+//          (chunk, t), chunks `bstride` bytes apart), or a zeroed 16-byte
+//          slot with bstride 0
 //   sb0/1  (scale | bias << 16) words of rows g and g + 8, one per group
 //   xg     per-group sums of the input (all columns in use, added)
+template <int LCPG>
 __device__ __forceinline__ void tile_task(uint32_t tile, TileGeom geo, int c0, int c1,
-                                          const uint8_t* bsrc, const uint32_t* sb0,
-                                          const uint32_t* sb1, const float* xg, int lcpg,
-                                          float& out0, float& out1) {
-  const int lane = threadIdx.x & 31, tg = lane & 3;
+                                          const uint8_t* bcol, uint32_t bstride,
+                                          const uint32_t* sb0, const uint32_t* sb1,
+                                          const float* xg, float& out0, float& out1) {
+  constexpr int CPG = 1 << LCPG;
+  constexpr int STEP = CPG < 2 ? 2 : CPG;  // chunks per iteration
+  // ldmatrix and mma are .aligned: the whole warp must arrive together (callers
+  // come here from per-lane waits and lane-0 copy issue)
+  __syncwarp();
+  const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const int r = (lane & 7) + 8 * (mi & 1), dc = mi >> 1;
   const uint32_t rbase = tile + (uint32_t)r * geo.pitch;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float o0 = 0.f, o1 = 0.f;
-  const int cmask = (1 << lcpg) - 1;
-  for (int c = c0; c < c1; c += 2) {
-    const int cc = c + dc;
-    uint32_t addr;
-    if (geo.swz)
-      addr = rbase + (uint32_t)(cc >> 3) * geo.cb_stride + ((uint32_t)((cc & 7) ^ (r & 7)) << 4);
-    else
-      addr = rbase + ((uint32_t)cc << 4);
-    uint32_t w[4];
-    ldsm_x4(addr, w[0], w[1], w[2], w[3]);  // (row g, c), (row g+8, c), (g, c+1), (g+8, c+1)
+  auto fold = [&](const float (&acc)[4], int gi) {
+    const uint32_t s0 = sb0[gi], s1 = sb1[gi];
+    const float X = xg[gi];
+    const float sc0 = bf16_lo(s0), sc1 = bf16_lo(s1);
+    o0 = fmaf(sc0, acc[0] + acc[1], fmaf(bf16_hi(s0) - 128.0f * sc0, X, o0));
+    o1 = fmaf(sc1, acc[2] + acc[3], fmaf(bf16_hi(s1) - 128.0f * sc1, X, o1));
+  };
+  for (int c = c0; c < c1; c += STEP) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int ch = c + h;
-      uint4 b = make_uint4(0u, 0u, 0u, 0u);
-      if (bsrc) b = *reinterpret_cast<const uint4*>(bsrc + ((size_t)ch * 4 + tg) * 16);
-      const uint32_t wg = w[2 * h], wg8 = w[2 * h + 1];
-      mma16816(acc, code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg, 1), code_pair(wg8, 1), b.x,
-               b.y);
-      mma16816(acc, code_pair(wg, 2), code_pair(wg8, 2), code_pair(wg, 3), code_pair(wg8, 3), b.z,
-               b.w);
-      if ((ch & cmask) == cmask) {  // the group of chunk ch is complete: fold it
-        const int gi = ch >> lcpg;
-        const uint32_t s0 = sb0[gi], s1 = sb1[gi];
-        const float X = xg[gi];
-        const float sc0 = bf16_lo(s0), sc1 = bf16_lo(s1);
-        o0 = fmaf(sc0, acc[0] + acc[1], fmaf(bf16_hi(s0) - 128.0f * sc0, X, o0));
-        o1 = fmaf(sc1, acc[2] + acc[3], fmaf(bf16_hi(s1) - 128.0f * sc1, X, o1));
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    for (int cp = 0; cp < STEP; cp += 2) {
+      const int cc = c + cp + dc;
+      const uint32_t addr =
+          geo.swz ? rbase + (uint32_t)(cc >> 3) * geo.cb_stride + ((uint32_t)((cc & 7) ^ (r & 7)) << 4)
+                  : rbase + ((uint32_t)cc << 4);
+      uint32_t w[4];
+      ldsm_x4(addr, w[0], w[1], w[2], w[3]);  // (row g, c), (row g+8, c), (g, c+1), (g+8, c+1)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ch = c + cp + h;
+        const uint4 b = *reinterpret_cast<const uint4*>(bcol + (size_t)ch * bstride);
+        const uint32_t wg = w[2 * h], wg8 = w[2 * h + 1];
+        const uint32_t wg4 = wg >> 4, wg84 = wg8 >> 4;
+        mma16816(acc, code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg4, 0), code_pair(wg84, 0),
+                 b.x, b.y);
+        mma16816(acc, code_pair(wg >> 8, 0), code_pair(wg8 >> 8, 0), code_pair(wg4 >> 8, 0),
+                 code_pair(wg84 >> 8, 0), b.z, b.w);
+        if (CPG == 1) {
+          fold(acc, ch);
+          acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        }
       }
     }
+    if (CPG > 1) fold(acc, c >> LCPG);
   }
   out0 = o0;
   out1 = o1;
@@ -295,23 +306,25 @@ struct DecRouter {
   } while (0)
 #endif
 
-template <int NJ, int V1>
+template <int NJ, int LCPG>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
+  constexpr int V1 = kMaxE / 256;  // logits per thread in the selection
   constexpr int H = NJ * 256;
   constexpr int HC = H / 32;           // 32-element chunks of x (K chunks of gate/up)
   constexpr int XW = H / 2;            // bf16 pairs of x
   constexpr int XP = (XW + kThreads - 1) / kThreads;
   constexpr int S = DecRouter<NJ>::S;
   constexpr int NCB = H / 256;         // 128-byte column blocks of a gate/up row
-  extern __shared__ __align__(1024) uint8_t sm_raw[];
-  // the 128-byte swizzle of the TMA tiles follows address bits 7..9: work
-  // from a 1024-byte aligned base (the plan reserves the slack)
-  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+  // No alignment is declared on purpose: the 128-byte swizzled TMA tiles
+  // need a 1024-byte aligned base, and with a declared alignment the
+  // compiler may take the padding below to be zero.  Pointer arithmetic on
+  // the shared array keeps every access LDS/STS; the plan reserves the slack.
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nC = gridDim.x, c = blockIdx.x;
   const int E = a.E, k = a.k, I = a.I, L = a.L;
-  const int lg = 31 - __clz(a.G);  // G is 32, 64 or 128
-  const int lcpg = lg - 5;         // log2 of chunks per group
+  constexpr int lg = LCPG + 5;     // log2 G; G is 32, 64 or 128
   const int HG = H >> lg, IG = I >> lg, IC = I / 32;
   const int need = min(k + 1, E);  // entries whose order the fast path certifies
   const int g4 = lane >> 2, tg = lane & 3;
@@ -324,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   int* s_sidx = reinterpret_cast<int*>(sm + a.sm.misc + 512);         // [33] ranked candidates
   float* s_sval = reinterpret_cast<float*>(sm + a.sm.misc + 648);     // [33]
   float* s_g = reinterpret_cast<float*>(sm + a.sm.misc + 784);        // shared gate
+  const uint8_t* s_zero = sm + a.sm.misc + 800;                       // 16 zero bytes
   float* s_part = reinterpret_cast<float*>(sm + a.sm.part);           // router slice sums
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + a.sm.hist);     // [kBins + 1]
   uint2* s_cand = reinterpret_cast<uint2*>(sm + a.sm.cand);           // [kCandCap]
@@ -348,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   const bool has_down = dt1 > dt0;  // at most one 16-row tile of y per CTA (the plan checks)
   const int r0 = 16 * dt0;
   // k-splits of whole groups and of an even number of chunks (ldmatrix takes two)
-  const int nsplit_gu = min(4, HC / max(2, 1 << lcpg)), nsplit_d = min(4, IC / max(2, 1 << lcpg));
+  const int nsplit_gu = min(4, HC / max(2, 1 << LCPG)), nsplit_d = min(4, IC / max(2, 1 << LCPG));
   const bool dswz = I / 2 >= 128;
   const int ncbd = dswz ? I / 256 : 1;
   const TileGeom geo_gu{16u * 128u, 128u, true};
@@ -413,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     for (int i = 0; i < kNumMbar; ++i) ptx::mbar_init(&mbar[i], 1);
     ptx::fence_mbar_init();
   }
+  if (tid < 4) reinterpret_cast<uint32_t*>(sm + a.sm.misc + 800)[tid] = 0u;
   __syncthreads();
   ptx::griddep_launch_dependents();
   if (tid == 0) {
@@ -580,8 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         const uint32_t* sb0 = ssb + (size_t)min(row0, 8 * nsu - 1) * HG;
         const uint32_t* sb1 = ssb + (size_t)min(row1, 8 * nsu - 1) * HG;
         float o0, o1;
-        tile_task(tile, geo_gu, sp * span, (sp + 1) * span, g4 == 0 ? s_xp : nullptr, sb0, sb1,
-                  s_xg, lcpg, o0, o1);
+        tile_task<LCPG>(tile, geo_gu, sp * span, (sp + 1) * span,
+                        g4 == 0 ? s_xp + tg * 16 : s_zero, g4 == 0 ? 64u : 0u, sb0, sb1, s_xg, o0,
+                        o1);
         if (tg == 0) {
           s_pgu[t * 16 + g4] = o0;
           s_pgu[t * 16 + g4 + 8] = o1;
@@ -815,8 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         const uint32_t* sb0 = gsb + (size_t)min(row0, 8 * nunit - 1) * HG;
         const uint32_t* sb1 = gsb + (size_t)min(row1, 8 * nunit - 1) * HG;
         float o0, o1;
-        tile_task(tile, geo_gu, sp * span, (sp + 1) * span, g4 == 0 ? s_xp : nullptr, sb0, sb1,
-                  s_xg, lcpg, o0, o1);
+        tile_task<LCPG>(tile, geo_gu, sp * span, (sp + 1) * span,
+                        g4 == 0 ? s_xp + tg * 16 : s_zero, g4 == 0 ? 64u : 0u, sb0, sb1, s_xg, o0,
+                        o1);
         if (tg == 0) {
           s_pgu[t * 16 + g4] = o0;
           s_pgu[t * 16 + g4 + 8] = o1;
@@ -886,11 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
                                                 : a.sm.dn + (uint32_t)j * a.sm.dn_expert);
         const uint32_t* sbt = reinterpret_cast<const uint32_t*>(
             shared ? pb + a.sm.b_sdsb : sm + a.sm.dn + (size_t)j * a.sm.dn_expert + a.sm.dn_sb);
-        const size_t boff = (size_t)j * IC * 64;  // expert j's permuted entries
-        const uint8_t* bs = g4 == 0 ? hp_hi + boff : g4 == 1 ? hp_lo + boff : nullptr;
+        const size_t boff = (size_t)j * IC * 64 + tg * 16;  // expert j's permuted entries
+        const uint8_t* bs = g4 == 0 ? hp_hi + boff : g4 == 1 ? hp_lo + boff : s_zero;
         float o0, o1;
-        tile_task(tile, geo_d, sp * span, (sp + 1) * span, bs, sbt + (size_t)g4 * IG,
-                  sbt + (size_t)(g4 + 8) * IG, hg + (size_t)j * IG, lcpg, o0, o1);
+        tile_task<LCPG>(tile, geo_d, sp * span, (sp + 1) * span, bs, g4 < 2 ? 64u : 0u,
+                        sbt + (size_t)g4 * IG, sbt + (size_t)(g4 + 8) * IG, hg + (size_t)j * IG,
+                        o0, o1);
         if (tg == 0) {
           s_pdn[t * 16 + g4] = o0;
           s_pdn[t * 16 + g4 + 8] = o1;
@@ -1033,7 +1051,7 @@ bool plan_smem(const Dims& d, int nC, bool chain, DecSmem& s) {
   return s.total <= 227 * 1024;
 }
 
-template <int NJ, int V1>
+template <int NJ, int LC>
 cudaError_t launch_t(const DecArgs& a, int nC, cudaStream_t st, bool coop) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nC);
@@ -1052,37 +1070,37 @@ cudaError_t launch_t(const DecArgs& a, int nC, cudaStream_t st, bool coop) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<NJ, V1>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<NJ, LC>, a);
 }
 
-template <int NJ, int V1>
+template <int NJ, int LC>
 cudaError_t prepare_t(int smem, int* occ) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NJ, V1>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NJ, LC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<NJ, V1>, kThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<NJ, LC>, kThreads,
                                                        smem);
 }
 
-template <int NJ, int V1>
+template <int NJ, int LC>
 struct PrepareF {
-  static cudaError_t run(int smem, int* occ) { return prepare_t<NJ, V1>(smem, occ); }
+  static cudaError_t run(int smem, int* occ) { return prepare_t<NJ, LC>(smem, occ); }
 };
-template <int NJ, int V1>
+template <int NJ, int LC>
 struct LaunchF {
   static cudaError_t run(const DecArgs* a, int nC, cudaStream_t st, bool coop) {
-    return launch_t<NJ, V1>(*a, nC, st, coop);
+    return launch_t<NJ, LC>(*a, nC, st, coop);
   }
 };
 
-// Dispatch over (H / 256) x (logits per thread of the selection).
+// Dispatch over (H / 256) x (log2 of 32-input chunks per group).
 template <template <int, int> class F, typename... Args>
 cudaError_t dispatch(const Dims& d, Args... args) {
-  const int v1 = d.E <= 256 ? 1 : d.E <= 512 ? 2 : 4;
+  const int lc = d.G == 32 ? 0 : d.G == 64 ? 1 : 2;
 #define MOE_DEC_CASE(NJ)                                                               \
   case NJ:                                                                             \
-    return v1 == 1 ? F<NJ, 1>::run(args...) : v1 == 2 ? F<NJ, 2>::run(args...)         \
-                                                      : F<NJ, 4>::run(args...);
+    return lc == 0 ? F<NJ, 0>::run(args...) : lc == 1 ? F<NJ, 1>::run(args...)         \
+                                                      : F<NJ, 2>::run(args...);
   switch (d.H / 256) {
     MOE_DEC_CASE(1)
     MOE_DEC_CASE(2)
