@@ -53,6 +53,10 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--path", type=int, default=0, help="kernel path (0 auto)")
+    p.add_argument("--mode", choices=["auto", "stack", "layers"], default="auto",
+                   help="one-token workloads: 'stack' chains the layers (RMSNorm + residual) "
+                        "in one persistent launch per token; 'layers' runs independent "
+                        "layers, one moe_forward each (auto: stack)")
     p.add_argument("--profile", action="store_true",
                    help="short run for profilers: no clock-warming loop, no end-to-end or "
                         "stage timing, no CPU baseline")
@@ -99,6 +103,8 @@ def peaks():
 # (profiles/traffic.json), with the hash of the sources they were taken on:
 # reported only while those sources are unchanged.
 TRAFFIC_SOURCES = {
+    "decode_kernel": ["decode.cu", "routing_common.cuh", "device_util.cuh", "sm100_ptx.cuh",
+                      "moe_internal.cuh"],
     "fused_decode_kernel": ["fused_decode.cu", "routing_common.cuh", "device_util.cuh",
                             "sm100_ptx.cuh", "moe_internal.cuh"],
     "grouped_gemm_kernel<gate/up>": ["prefill.cu", "device_util.cuh", "sm100_ptx.cuh",
@@ -225,9 +231,17 @@ def run_reference(args, wl):
     n_layers = min(L, 2)
     Ws = [synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s) for l in range(n_layers)]
     tok = 1 if wl.T == 1 else min(wl.T, 8)
+    stacked = stack_mode(args, wl)
+    norms = stack_norm_weights(wl, n_layers)
+    state = {"x": synth.tokens(0, wl.wid, 0, 0, 1, wl.H)[0]}
 
     def step(i):
         l = i % n_layers
+        if stacked:  # one layer of the residual stack: RMSNorm, block, residual add
+            n = O.rms_norm(state["x"], norms[l], STACK_EPS)
+            r = O.moe_block(n[None, :], Ws[l], wl.k, wl.G)
+            state["x"] = O.residual_add(state["x"], r["y"][0])
+            return
         x = synth.tokens(0, wl.wid, l, i // n_layers, wl.T, wl.H)
         O.moe_block(x, Ws[l], wl.k, wl.G, tokens=list(range(tok)))
 
@@ -238,13 +252,14 @@ def run_reference(args, wl):
         step(args.warmup + i)
     dt = time.perf_counter() - t0
     value = args.steps * tok / dt
-    sample = f"each step: {tok} token(s) through one MoE layer (layers 0..{n_layers - 1} alternate)"
+    sample = (f"each step: {tok} token(s) through one MoE layer (layers 0..{n_layers - 1} "
+              "alternate)" + (", with the stack's RMSNorm and residual add" if stacked else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": config_of(wl, L),
+        "config": config_of(wl, L, stacked),
         "note": "CPU oracle (numpy float64), a bounded sample of the workload per step",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                          "sample": sample},
@@ -253,11 +268,25 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, L):
+def stack_mode(args, wl):
+    return wl.T == 1 and args.mode in ("auto", "stack")
+
+
+STACK_EPS = 1e-6
+
+
+def stack_norm_weights(wl, L):
+    """Seeded RMSNorm weights of the stack, bf16 bits ~ N(1, 0.1^2) (synthetic)."""
+    return [synth.norm_weights(0, wl.wid, l, wl.H) for l in range(L)]
+
+
+def config_of(wl, L, stacked):
     """The workload's description; both arms print the same dict."""
     return {"workload": wl.name, "E": wl.E, "k": wl.k, "hidden": wl.H, "inter": wl.I,
             "shared_inter": wl.Is, "group": wl.G, "tokens_per_step": wl.T, "layers": L,
             "zipf_s": wl.zipf_s,
+            "chaining": "layer l+1 consumes RMSNorm(x_l + y_l) (residual stack)" if stacked
+                        else "independent layers, each with its own seeded input",
             "weights": "int4 affine (bf16 scale+bias per group), seeded synthetic",
             "parallelism": "replicas",
             "l2": "inputs larger than L2: every step streams distinct expert weights "
@@ -474,7 +503,7 @@ def run_ours(args, wl):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if grouped else "fp32", "data": "synthetic",
-        "config": config_of(wl, L),
+        "config": config_of(wl, L, False),
         "note": f"each step touches {unique_per_step / 1e6:.0f} MB of distinct expert weights; "
                 f"{S} distinct step inputs rotate",
         "us_per_layer": us_layer, "stack_tokens_per_s": world * T / (ms_step / 1e3),
@@ -495,11 +524,185 @@ def run_ours(args, wl):
         torch.distributed.destroy_process_group()
 
 
+def run_ours_stack(args, wl):
+    """One token per step through the whole residual stack: one persistent
+    launch (moe_stack_forward) per step."""
+    import torch
+
+    import int4_routed_expert_decode_gb300 as moe
+    from int4_routed_expert_decode_gb300 import build as moe_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    moe_build.build()
+    L = args.layers or wl.layers
+    H = wl.H
+    S = max(1, min(args.distinct, args.steps + args.warmup))
+    layers = []
+    for l in range(L):
+        W = synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s)
+        layers.append(moe.MoELayer(wl.E, wl.k, H, wl.I, wl.Is, wl.G, weights=W, max_T=1))
+        del W
+    norms = [torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16)
+             for g in stack_norm_weights(wl, L)]
+    stack = moe.MoEStack(layers, norms, STACK_EPS)
+    x_all = torch.empty((S, H), dtype=torch.bfloat16, device="cuda")
+    for s in range(S):
+        x_all[s].copy_(torch.from_numpy(synth.tokens(0, wl.wid, 0, s, 1, H)[0].view(np.int16))
+                       .view(torch.bfloat16))
+    x_out = torch.empty((H,), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((L, H), dtype=torch.bfloat16, device="cuda")
+    xn = torch.empty((L, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((L, wl.k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((L, wl.k), dtype=torch.float32, device="cuda")
+    x_in = torch.empty((H,), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def enqueue(xsrc):
+        moe.moe_stack_forward(stack.stack, xsrc, None, x_out, y, xn, idx, wts,
+                              stream=stream.cuda_stream)
+
+    uniq_bytes = []
+    first = None
+    with torch.cuda.stream(stream):
+        for s in range(S):
+            enqueue(x_all[s])
+            stream.synchronize()
+            if s == 0:
+                first = (y.clone(), xn.clone(), idx.clone())
+            ids = idx.cpu().numpy()
+            uniq_bytes.append(sum(len(set(ids[l].tolist())) * wl.expert_bytes + wl.shared_bytes
+                                  for l in range(L)))
+    st = stack.status(stream.cuda_stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"stack: {moe.moe_status_string(st)}")
+    unique_per_step = float(np.mean(uniq_bytes))
+
+    clocks = ClockSampler(local).start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            enqueue(x_all[i % S])
+        stream.synchronize()
+        t_load = time.perf_counter()
+        i = 0
+        while not args.profile and time.perf_counter() - t_load < 1.0:
+            enqueue(x_all[i % S])
+            i += 1
+            if i % 16 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            enqueue(x_all[(args.warmup + i) % S])
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    st = stack.status(stream.cuda_stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"stack (timed): {moe.moe_status_string(st)}")
+    t_max = max_over_ranks(ms, world, "cuda")
+    value = job_throughput(t_max, world, 1, L, args.steps)
+    ms_step = t_max / args.steps
+    us_layer = ms_step * 1e3 / L
+    hbm = unique_per_step / (ms_step / 1e3) / 1e9
+    pk = peaks()
+
+    # e2e through the C ABI with host buffers: H2D x, the launch, D2H x_out every step
+    x_host = torch.empty((H,), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x_all[0].cpu())
+    out_host = torch.empty((H,), dtype=torch.bfloat16, pin_memory=True)
+    k_e2e = 1 if args.profile else max(1, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x_in.copy_(x_host, non_blocking=True)
+            enqueue(x_in)
+            out_host.copy_(x_out, non_blocking=True)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            x_in.copy_(x_host, non_blocking=True)
+            enqueue(x_in)
+            out_host.copy_(x_out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / k_e2e
+    e2e_value = world * L / (ms_e2e / 1e3)
+
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
+        v, n, dt, sample, _ = oracle_units(wl, args.cpu_budget, L)
+        cpu = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+               "sample": sample + f", {dt:.1f} s"}
+        # layers 0 and L-1 of the first step against the oracle on the GPU's block input
+        from oracle import moe_oracle as O
+        y0, xn0, idx0 = first
+        errs, idx_ok = [], True
+        for l in sorted({0, L - 1}):
+            W = synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s)
+            nb = xn0[l].view(torch.int16).cpu().numpy().view(np.uint16)
+            r = O.moe_block(nb[None, :], W, wl.k, wl.G)
+            yg = y0[l].float().cpu().numpy().astype(np.float64)
+            errs.append(float(np.abs(yg - r["y"][0]).max() / np.abs(r["y"][0]).max()))
+            idx_ok = idx_ok and idx0[l].cpu().numpy().tolist() == r["topk_idx"][0].tolist()
+        parity = {"checked_layers": sorted({0, L - 1}), "max_rel_err": max(errs),
+                  "topk_idx_equal": idx_ok}
+
+    P = wl.k
+    flops_layer = 2.0 * H * (3 * wl.I * P + 3 * wl.Is + wl.E)
+    algo_bytes_layer = unique_per_step / L + wl.router_bytes + 2 * H * 2
+    achieved = algo_bytes_layer / (us_layer * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": measured_traffic("decode_kernel", wl.name),
+                "kernel": f"decode_kernel, {L} layers per launch, "
+                          f"{algo_bytes_layer / 1e6:.2f} MB algorithmic per layer "
+                          f"({us_layer:.2f} us per layer)",
+                "peak_source": pk["source"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": config_of(wl, L, True),
+        "note": f"each step touches {unique_per_step / 1e6:.0f} MB of distinct expert weights; "
+                f"{S} distinct step inputs rotate; one launch per step for all {L} layers",
+        "us_per_layer": us_layer, "stack_tokens_per_s": world / (ms_step / 1e3),
+        "hbm_gbs_unique_expert_bytes": hbm, "hbm_frac": hbm / pk["hbm_gbs"],
+        "tflops_layer": flops_layer / (us_layer * 1e-6) / 1e12,
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": H * 2,
+                "d2h_bytes_per_step": H * 2},
+        "clocks": clk, "gpu_launches": args.steps,
+        "parity_spot_check": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    stack.close()
+    for layer in layers:
+        layer.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif stack_mode(args, wl):
+        run_ours_stack(args, wl)
     else:
         run_ours(args, wl)
 

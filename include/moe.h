@@ -243,6 +243,71 @@ int moe_route_static(const void* x, int T, const uint16_t* router_w, const float
                      const uint16_t* shared_gate_w, int E, int k, int hidden, int32_t* topk_idx,
                      float* topk_w, float* shared_gate, void* stream);
 
+/* ---------------------------------------------------------------- stacks
+ * A stack chains L MoE layers of one shape for ONE token in a single
+ * persistent launch, as a decoder runs them one after another (the Swiftlet
+ * README on the wpnews page, paragraph "Status": the decode loop is bound by
+ * dispatch, not by IO).  There is no attention between the blocks here:
+ * layer l's input is the previous residual, normalised, and its output is
+ * added back:
+ *
+ *   n_l     = bf16( x_l / sqrt(mean_h x_l[h]^2 + eps) * norm_w_l )   RMSNorm
+ *   y_l     = MoE block of layer l on n_l (as moe_forward, T = 1)
+ *   x_{l+1} = bf16( x_l + y_l )                       residual (y_l in bf16)
+ *
+ * with x_0 the caller's x and x_L the result.  The RMSNorm runs in fp32 (the
+ * sum of squares in a fixed order, so results are reproducible bit for bit).
+ *
+ * The launch is cooperative: all of its CTAs, one per SM, must be resident
+ * together, and it fails with MOE_ERR_CUDA rather than start otherwise
+ * (other work occupying SMs, MPS limits).  Its CTAs exchange data through
+ * counters in the stack's workspace that only grow (each launch reads the
+ * launch count afresh), so a CUDA graph captured around moe_stack_forward
+ * replays correctly, also after moe_stack_get_status has reset the counters.
+ * A stack borrows its layers' weights: destroy it before any of them, and
+ * do not reload their weights while it exists.  One stack runs on one
+ * stream at a time (its launches must be ordered). */
+#define MOE_STACK_MAX_LAYERS 1024
+typedef struct moe_stack moe_stack;
+
+/* Create a stack over `layers` [L] (L in [1, MOE_STACK_MAX_LAYERS]), every
+ * one created with the same sizes on the same device and already loaded
+ * (moe_reserve is not needed).
+ *   norm_w  NULL, or L device pointers (16-byte aligned) to bf16 [hidden]
+ *           RMSNorm weights; a NULL entry means all ones
+ *   eps     RMSNorm epsilon in (0, 1)
+ * Errors: INVALID_ARG (pointers, L, eps, mismatched layers), NOT_LOADED,
+ * UNSUPPORTED (sizes the persistent kernel does not fit: hidden up to 2048,
+ * inter == shared_inter, shared memory), OOM, CUDA.  Messages go to
+ * moe_last_error(NULL). */
+int moe_stack_create(moe_ctx* const* layers, int L, const uint16_t* const* norm_w, float eps,
+                     moe_stack** out);
+
+/* Run the stack for one token (asynchronous on `stream`, no allocation).
+ *   x                   bf16 [hidden] device, 16-byte aligned, read
+ *   expert_slot_tables  int32 [L][E] device, or NULL for identity tables
+ *                       (every layer needs n_slots >= E); as moe_forward
+ *   x_out               bf16 [hidden] device, or NULL: x_L; may equal x
+ *   y                   bf16 [L][hidden] device, or NULL: every y_l
+ *   xn                  bf16 [L][hidden] device, or NULL: every n_l
+ *   topk_idx, topk_w    int32 / fp32 [L][k] device, written as moe_forward
+ * Errors (host side): INVALID_ARG, CUDA (launch failure, including a grid
+ * that cannot be co-resident).  Device errors are sticky: see
+ * moe_stack_get_status. */
+int moe_stack_forward(moe_stack* s, const void* x, const int32_t* expert_slot_tables, void* x_out,
+                      void* y, void* xn, int32_t* topk_idx, float* topk_w, void* stream);
+
+/* As moe_get_status, for the stack's own error word; after a device error it
+ * also zeroes the stack's exchange counters (synchronous). */
+int moe_stack_get_status(moe_stack* s, void* stream);
+
+/* As moe_set_test_flags: MOE_TEST_WAIT_TIMEOUT makes every layer's logits
+ * exchange wait for one arrival more than the grid has. */
+int moe_stack_set_test_flags(moe_stack* s, int flags);
+
+/* Free the stack's device memory (synchronises the device).  NULL is a no-op. */
+void moe_stack_destroy(moe_stack* s);
+
 const char* moe_last_error(const moe_ctx* ctx);
 const char* moe_status_string(int status);
 

@@ -36,7 +36,8 @@ EXPORTS = (
     "moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
     "moe_read_expert", "moe_set_path", "moe_expert_blob_bytes", "moe_device_bytes",
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
-    "moe_route_static", "moe_set_test_flags", "moe_set_stage_events",
+    "moe_route_static", "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
+    "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags", "moe_stack_destroy",
 )
 
 
@@ -96,9 +97,17 @@ def lib():
     L.moe_destroy.restype = None
     L.moe_route_static.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     L.moe_route_static.restype = i32
+    L.moe_stack_create.argtypes = [ctypes.POINTER(vp), i32, ctypes.POINTER(vp), ctypes.c_float,
+                                   ctypes.POINTER(vp)]
+    L.moe_stack_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_stack_get_status.argtypes = [vp, vp]
+    L.moe_stack_set_test_flags.argtypes = [vp, i32]
+    L.moe_stack_destroy.argtypes = [vp]
+    L.moe_stack_destroy.restype = None
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
                  "moe_read_expert", "moe_set_path", "moe_last_launch_count",
-                 "moe_set_test_flags", "moe_set_stage_events"):
+                 "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
+                 "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -261,7 +270,87 @@ def moe_route_static(x, T: int, router_w, router_bias, shared_gate_w, E: int, k:
                                   _addr(topk_w), _addr(shared_gate), _stream(stream)))
 
 
+def moe_stack_create(layer_ctxs, norm_w=None, eps: float = 1e-6) -> int:
+    """A stack over contexts `layer_ctxs` (see include/moe.h); norm_w: None or a
+    list of device bf16 [H] tensors / addresses (None entries: all ones)."""
+    n = len(layer_ctxs)
+    ctxs = (ctypes.c_void_p * n)(*layer_ctxs)
+    norms = None
+    if norm_w is not None:
+        norms = (ctypes.c_void_p * n)(*[_addr(w) for w in norm_w])
+    out = ctypes.c_void_p()
+    _check(lib().moe_stack_create(ctxs, n, norms, ctypes.c_float(eps), ctypes.byref(out)))
+    return out.value
+
+
+def moe_stack_forward(stack: int, x, expert_slot_tables, x_out, y, xn, topk_idx, topk_w,
+                      stream=None):
+    _check(lib().moe_stack_forward(stack, _addr(x), _addr(expert_slot_tables), _addr(x_out),
+                                   _addr(y), _addr(xn), _addr(topk_idx), _addr(topk_w),
+                                   _stream(stream)))
+
+
+def moe_stack_get_status(stack: int, stream=None) -> int:
+    """Synchronise and return the stack's sticky device status (does not raise)."""
+    return lib().moe_stack_get_status(stack, _stream(stream))
+
+
+def moe_stack_set_test_flags(stack: int, flags: int):
+    _check(lib().moe_stack_set_test_flags(stack, flags))
+
+
+def moe_stack_destroy(stack: int):
+    lib().moe_stack_destroy(stack)
+
+
 # ----------------------------------------------------------------- convenience
+class MoEStack:
+    """L loaded MoELayers of one shape chained for one token in one launch.
+
+    ``forward(x)`` takes a CUDA bf16 tensor [H] and returns (x_out [H],
+    y [L, H], xn [L, H], topk_idx [L, k], topk_w [L, k]).
+    """
+
+    def __init__(self, layers, norm_w=None, eps: float = 1e-6):
+        self.layers = list(layers)  # kept alive: the stack borrows their weights
+        self.L = len(self.layers)
+        l0 = self.layers[0]
+        self.H, self.k, self.E = l0.H, l0.k, l0.E
+        self.norm_w = norm_w
+        self.stack = moe_stack_create([l.ctx for l in self.layers], norm_w, eps)
+
+    def forward(self, x, tables=None, x_out=None, y=None, xn=None, topk_idx=None, topk_w=None,
+                stream=None):
+        import torch
+        dev = x.device
+        if x_out is None:
+            x_out = torch.empty((self.H,), dtype=torch.bfloat16, device=dev)
+        if y is None:
+            y = torch.empty((self.L, self.H), dtype=torch.bfloat16, device=dev)
+        if xn is None:
+            xn = torch.empty((self.L, self.H), dtype=torch.bfloat16, device=dev)
+        if topk_idx is None:
+            topk_idx = torch.empty((self.L, self.k), dtype=torch.int32, device=dev)
+        if topk_w is None:
+            topk_w = torch.empty((self.L, self.k), dtype=torch.float32, device=dev)
+        moe_stack_forward(self.stack, x, tables, x_out, y, xn, topk_idx, topk_w, stream)
+        return x_out, y, xn, topk_idx, topk_w
+
+    def status(self, stream=None) -> int:
+        return moe_stack_get_status(self.stack, stream)
+
+    def close(self):
+        if self.stack:
+            moe_stack_destroy(self.stack)
+            self.stack = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class MoELayer:
     """One MoE layer: a context with its weights and workspace.
 

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/moe.h: argument checks, device
 // memory, weight loading/repacking and the launch sequence of moe_forward.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -11,6 +12,21 @@ using namespace moe;
 
 struct moe_ctx {
   Ctx c;
+};
+
+struct moe_stack {
+  int device = -1;
+  Dims d{};
+  int L = 0;
+  int num_sms = 0;
+  int n_slots_min = 1 << 30;  // smallest n_slots over the layers
+  float eps = 1e-6f;
+  int test_flags = 0;
+  void* base = nullptr;       // one device allocation: descriptors, workspace, error word
+  DecLayer* layers = nullptr;  // [L]
+  DecWorkspace ws{};
+  int32_t* err = nullptr;
+  unsigned long long* stamps = nullptr;  // phase timestamps (instrumented builds only)
 };
 
 namespace {
@@ -72,11 +88,10 @@ void free_workspace(Ctx& c) {
   c.dec_ok = 0;
 }
 
-// The descriptor the persistent decode kernel reads for this layer (written
-// once the weights and the workspace both exist).
-cudaError_t refresh_decode_layer(Ctx& c) {
-  if (!c.pool || !c.dec_layer) return cudaSuccess;
-  DecLayer D{};
+// The descriptor of this layer for the persistent decode kernel (host copy;
+// false if a TMA map could not be encoded).
+bool fill_decode_layer(const Ctx& c, DecLayer& D) {
+  D = DecLayer{};
   D.router_w = c.router_w;
   D.prior = c.router_bias;
   D.shared_gate_w = c.shared_gate_w;
@@ -91,8 +106,15 @@ cudaError_t refresh_decode_layer(Ctx& c) {
   D.d_q = c.ex.d_q;
   D.d_sb = c.ex.d_sb;
   D.n_slots = c.n_slots;
-  if (c.dec_ok && !decode_encode_maps(c.d, c.pool, c.ex, c.n_slots, c.shared, c.sh, &D))
-    return cudaErrorInvalidValue;
+  return decode_encode_maps(c.d, c.pool, c.ex, c.n_slots, c.shared, c.sh, &D);
+}
+
+// The descriptor the persistent decode kernel reads for this layer (written
+// once the weights and the workspace both exist).
+cudaError_t refresh_decode_layer(Ctx& c) {
+  if (!c.pool || !c.dec_layer || !c.dec_ok) return cudaSuccess;
+  DecLayer D;
+  if (!fill_decode_layer(c, D)) return cudaErrorInvalidValue;
   return cudaMemcpy(c.dec_layer, &D, sizeof D, cudaMemcpyHostToDevice);
 }
 
@@ -370,8 +392,8 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.n_tiles = (int32_t*)(base + o_ntiles);
   c.dec_layer = (DecLayer*)(base + o_dlayer);
 #ifdef MOE_DECODE_STAMPS
-  cudaMalloc(&c.dec_stamps, (size_t)n_sms * 16 * 8);
-  cudaMemset(c.dec_stamps, 0, (size_t)n_sms * 16 * 8);
+  cudaMalloc(&c.dec_stamps, (size_t)n_sms * 32 * 8);
+  cudaMemset(c.dec_stamps, 0, (size_t)n_sms * 32 * 8);
 #endif
   decode_workspace_carve(d, n_sms, base + o_dws, &c.dec_ws);
   c.max_T = max_T;
@@ -485,6 +507,10 @@ int moe_get_status(moe_ctx* ctx, void* stream) {
     // a timed-out grid barrier leaves its counter off the multiple of the
     // grid size that every barrier expects: start it afresh
     if (ctx->c.ws.bar) cudaMemset(ctx->c.ws.bar, 0, kSyncWords * 8);
+    // the persistent decode kernel's exchanges: launch counters and arrival
+    // counters back to zero together (a launch reads both afresh, so CUDA
+    // graphs captured earlier replay correctly after the reset)
+    if (ctx->c.dec_ws.seq) decode_workspace_reset(ctx->c.num_sms, ctx->c.dec_ws);
     return set_msg(ctx, v, "device reported: %s", moe_status_string(v));
   }
   return MOE_OK;
@@ -584,11 +610,172 @@ void moe_destroy(moe_ctx* ctx) {
   delete ctx;
 }
 
+// ---------------------------------------------------------------- stacks
+// moe_stack_*: L layers of one shape run for one token by a single
+// cooperative launch of the persistent decode kernel.
+
+int moe_stack_create(moe_ctx* const* layers, int L, const uint16_t* const* norm_w, float eps,
+                     moe_stack** out) {
+  if (!out) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!layers || L < 1 || L > MOE_STACK_MAX_LAYERS)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "layers is NULL or L=%d not in [1, %d]", L,
+                   MOE_STACK_MAX_LAYERS);
+  if (!(eps > 0.f) || !(eps < 1.f))
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "eps must lie in (0, 1)");
+  for (int l = 0; l < L; ++l) {
+    if (!layers[l]) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "layers[%d] is NULL", l);
+    const Ctx& c = layers[l]->c;
+    if (!c.pool) return set_msg(nullptr, MOE_ERR_NOT_LOADED, "layers[%d] has no weights", l);
+    const Dims& a = layers[0]->c.d;
+    if (c.d.E != a.E || c.d.k != a.k || c.d.H != a.H || c.d.I != a.I || c.d.Is != a.Is ||
+        c.d.G != a.G || c.device != layers[0]->c.device)
+      return set_msg(nullptr, MOE_ERR_INVALID_ARG,
+                     "layers[%d] differs from layers[0] in shape or device", l);
+    if (norm_w && norm_w[l] && ((uintptr_t)norm_w[l] & 15) != 0)
+      return set_msg(nullptr, MOE_ERR_INVALID_ARG, "norm_w[%d] must be 16-byte aligned", l);
+  }
+  const Ctx& c0 = layers[0]->c;
+  DeviceGuard guard(c0.device);
+  int nC = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&nC, cudaDevAttrMultiProcessorCount, c0.device);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "device attributes");
+  int ok = 0;
+  if ((e = decode_prepare(c0.d, nC, true, &ok)) != cudaSuccess)
+    return cuda_fail(nullptr, e, "kernel attributes");
+  if (!ok)
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED,
+                   "the persistent decode kernel does not fit these sizes (hidden %d, inter %d, "
+                   "shared_inter %d, E %d, k %d)",
+                   c0.d.H, c0.d.I, c0.d.Is, c0.d.E, c0.d.k);
+  moe_stack* s = new (std::nothrow) moe_stack;
+  if (!s) return set_msg(nullptr, MOE_ERR_OOM, "host allocation");
+  s->device = c0.device;
+  s->d = c0.d;
+  s->L = L;
+  s->num_sms = nC;
+  s->eps = eps;
+  for (int l = 0; l < L; ++l) s->n_slots_min = std::min(s->n_slots_min, layers[l]->c.n_slots);
+  const size_t b_layers = align256((uint64_t)L * sizeof(DecLayer));
+  const size_t b_ws = decode_workspace_bytes(c0.d, nC);
+  e = cudaMalloc(&s->base, b_layers + b_ws + 256);
+  if (e != cudaSuccess) {
+    delete s;
+    return cuda_fail(nullptr, e, "stack workspace");
+  }
+  uint8_t* base = (uint8_t*)s->base;
+  s->layers = (DecLayer*)base;
+  decode_workspace_carve(c0.d, nC, base + b_layers, &s->ws);
+  s->err = (int32_t*)(base + b_layers + b_ws);
+  DecLayer* host = new (std::nothrow) DecLayer[L];
+  bool good = host != nullptr;
+  for (int l = 0; good && l < L; ++l) {
+    good = fill_decode_layer(layers[l]->c, host[l]);
+    host[l].norm_w = norm_w ? norm_w[l] : nullptr;
+  }
+  if (good) {
+    e = cudaMemset(s->base, 0, b_layers + b_ws + 256);
+    if (e == cudaSuccess) e = cudaMemcpy(s->layers, host, (size_t)L * sizeof(DecLayer),
+                                         cudaMemcpyHostToDevice);
+  }
+  delete[] host;
+  if (!good || e != cudaSuccess) {
+    cudaFree(s->base);
+    delete s;
+    return good ? cuda_fail(nullptr, e, "stack descriptors")
+                : set_msg(nullptr, MOE_ERR_CUDA, "TMA descriptor encoding failed");
+  }
+#ifdef MOE_DECODE_STAMPS
+  cudaMalloc(&s->stamps, (size_t)L * nC * 32 * 8);
+  cudaMemset(s->stamps, 0, (size_t)L * nC * 32 * 8);
+#endif
+  *out = s;
+  return MOE_OK;
+}
+
+int moe_stack_forward(moe_stack* s, const void* x, const int32_t* expert_slot_tables, void* x_out,
+                      void* y, void* xn, int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!s) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "stack is NULL");
+  if (!x || !topk_idx || !topk_w)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "x, topk_idx and topk_w must be non-NULL");
+  if (((uintptr_t)x & 15) != 0 || ((uintptr_t)x_out & 15) != 0 || ((uintptr_t)y & 15) != 0 ||
+      ((uintptr_t)xn & 15) != 0)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "x, x_out, y and xn must be 16-byte aligned");
+  if (!expert_slot_tables && s->n_slots_min < s->d.E)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG,
+                   "identity slot tables need n_slots (%d) >= E (%d) in every layer",
+                   s->n_slots_min, s->d.E);
+  DeviceGuard guard(s->device);
+  DecLaunch p{};
+  p.layers = s->layers;
+  p.L = s->L;
+  p.x = (const uint16_t*)x;
+  p.x_out = (uint16_t*)x_out;
+  p.y = (uint16_t*)y;
+  p.xn_out = (uint16_t*)xn;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.tables = expert_slot_tables;
+  p.chain = 1;
+  p.eps = s->eps;
+  p.ws = s->ws;
+  p.err = s->err;
+  p.timeout_hook = s->test_flags & MOE_TEST_WAIT_TIMEOUT;
+  p.stamps = s->stamps;
+  // every CTA of the grid exchanges data with every other: the cooperative
+  // attribute makes the launch fail rather than start with CTAs not resident
+  p.cooperative = true;
+  const cudaError_t e = decode_launch(s->d, s->num_sms, p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "moe_stack_forward launch");
+  return MOE_OK;
+}
+
+int moe_stack_get_status(moe_stack* s, void* stream) {
+  if (!s) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "stack is NULL");
+  DeviceGuard guard(s->device);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "stream synchronise");
+  int32_t v = 0;
+  e = cudaMemcpy(&v, s->err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "status read");
+  if (v != 0) {
+    cudaMemset(s->err, 0, 4);
+    decode_workspace_reset(s->num_sms, s->ws);
+    return set_msg(nullptr, v, "device reported: %s", moe_status_string(v));
+  }
+  return MOE_OK;
+}
+
+int moe_stack_set_test_flags(moe_stack* s, int flags) {
+  if (!s) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "stack is NULL");
+  if (flags & ~MOE_TEST_WAIT_TIMEOUT)
+    return set_msg(nullptr, MOE_ERR_INVALID_ARG, "unknown test flags 0x%x", flags);
+  s->test_flags = flags;
+  return MOE_OK;
+}
+
+void moe_stack_destroy(moe_stack* s) {
+  if (!s) return;
+  {
+    DeviceGuard guard(s->device);
+    cudaDeviceSynchronize();
+    if (s->base) cudaFree(s->base);
+    if (s->stamps) cudaFree(s->stamps);
+  }
+  delete s;
+}
+
 }  // extern "C"
 
 #ifdef MOE_DECODE_STAMPS
+extern "C" int moe_debug_stack_stamps(moe_stack* s, unsigned long long* host, int n) {
+  if (!s || !s->stamps) return MOE_ERR_INVALID_ARG;
+  return cudaMemcpy(host, s->stamps, (size_t)n * 8, cudaMemcpyDeviceToHost) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
 // Instrumented builds only: the per-CTA phase timestamps of the last decode
-// launch ([CTA][8] nanoseconds of %globaltimer) and the launch attribute knob.
+// launch ([CTA][32] SM cycle counts) and the launch attribute knob.
 extern "C" int moe_debug_decode_stamps(moe_ctx* ctx, unsigned long long* host, int n) {
   if (!ctx || !ctx->c.dec_stamps) return MOE_ERR_INVALID_ARG;
   return cudaMemcpy(host, ctx->c.dec_stamps, (size_t)n * 8, cudaMemcpyDeviceToHost) == cudaSuccess

@@ -81,6 +81,7 @@ struct DecArgs {
   const uint16_t* x;     // layer-0 input [H]
   uint16_t* x_out;       // residual after the last layer [H], or null
   uint16_t* y;           // [L][H] per-layer block outputs, or null
+  uint16_t* xn_out;      // [L][H] per-layer block inputs, or null
   int32_t* topk_idx;     // [L][k]
   float* topk_w;         // [L][k]
   int32_t* perm;         // layer 0 only, or null
@@ -108,8 +109,12 @@ __device__ __forceinline__ int part(int n, int p, uint64_t inv_nc) {
   return udiv((uint32_t)n * (uint32_t)p, inv_nc);
 }
 
+// Waits sleep in hardware (100 us per try, at most ~1 s in all) so that the
+// warps still computing keep the issue slots.
 __device__ __forceinline__ void wait_mbar(uint64_t* bar, uint32_t parity, int32_t* err) {
-  if (!ptx::mbar_wait(bar, parity, 1u << 22)) record_error(err, MOE_ERR_TIMEOUT);
+  for (int i = 0; i < 10000; ++i)
+    if (ptx::mbar_try_wait_sleep(bar, parity, 100000u)) return;
+  record_error(err, MOE_ERR_TIMEOUT);
 }
 
 // This CTA's writes so far (every thread's, ordered by the barrier) become
@@ -176,12 +181,14 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
   return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
 }
 
-// Shared-memory layout of one tile of 16 rows for ldmatrix: the TMA wrote
-// column blocks of `pitch` bytes per row; with the 128-byte swizzle (pitch
-// 128) the 16-byte piece j of row r sits at piece j ^ (r & 7).
+// Shared-memory layout of one tile of 16 rows for ldmatrix: rows 0-7 and
+// 8-15 are two halves `half` bytes apart, each written by the TMA as column
+// blocks of 8 rows x `pitch` bytes; with the 128-byte swizzle (pitch 128)
+// the 16-byte piece j of row r sits at piece j ^ (r & 7).
 struct TileGeom {
-  uint32_t cb_stride;  // bytes between column blocks of the tile (16 rows x pitch)
+  uint32_t cb_stride;  // bytes between column blocks
   uint32_t pitch;      // bytes of one row in one column block (128, or less unswizzled)
+  uint32_t half;       // bytes between rows r and r + 8
   bool swz;
 };
 
@@ -208,7 +215,7 @@ __device__ __forceinline__ void tile_task(uint32_t tile, TileGeom geo, int c0, i
   const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const int r = (lane & 7) + 8 * (mi & 1), dc = mi >> 1;
-  const uint32_t rbase = tile + (uint32_t)r * geo.pitch;
+  const uint32_t rbase = tile + (uint32_t)(r >> 3) * geo.half + (uint32_t)(r & 7) * geo.pitch;
   float o0 = 0.f, o1 = 0.f;
   auto fold = [&](const float (&acc)[4], int gi) {
     const uint32_t s0 = sb0[gi], s1 = sb1[gi];
@@ -250,7 +257,7 @@ __device__ __forceinline__ void tile_task(uint32_t tile, TileGeom geo, int c0, i
 }
 
 // Logits read back from shared memory with one uniform bound, for the exact
-// fallback routine.
+// selection routine.
 struct SmemLogits {
   const float* l;
   float b;
@@ -260,25 +267,6 @@ struct SmemLogits {
   }
   __device__ __forceinline__ int id(int e) const { return e; }
 };
-
-// Near-ties or an overfull candidate set: the full exact selection by one
-// warp (out of line, rarely executed).
-template <int MAXV>
-__device__ __noinline__ void select_exact(const float* slog, float beta, int E, int k,
-                                          const uint16_t* xn, const uint16_t* router_w,
-                                          const float* prior, int H, uint8_t* scratch,
-                                          int* out_idx, float* out_val) {
-  int* si;
-  float* sv;
-  topk_select_warp_src<MAXV>(SmemLogits{slog, beta}, E, k, xn, router_w, prior, H, scratch, &si,
-                             &sv);
-  const int lane = threadIdx.x & 31;
-  if (lane < k) {
-    out_idx[lane] = si[lane];
-    out_val[lane] = sv[lane];
-  }
-  __syncwarp();
-}
 
 // Router summation of the decode kernel: a row is cut into S = min(8, NJ)
 // slices of NJ / S chunks; a lane sums each 8-element chunk with 8 sequential
@@ -295,10 +283,12 @@ struct DecRouter {
 };
 
 #ifdef MOE_DECODE_STAMPS
-#define STAMP(s)                                                                          \
-  do {                                                                                    \
-    if (a.stamps && threadIdx.x == 0)                                                     \
-      a.stamps[((size_t)l * gridDim.x + blockIdx.x) * 16 + (s)] = ptx::globaltimer_ns();  \
+// Instrumented builds: thread 0's SM cycle counter at phase s of layer l
+// (32 slots per layer and CTA).
+#define STAMP(s)                                                                     \
+  do {                                                                               \
+    if (a.stamps && threadIdx.x == 0)                                                \
+      a.stamps[((size_t)l * gridDim.x + blockIdx.x) * 32 + (s)] = clock64();         \
   } while (0)
 #else
 #define STAMP(s) \
@@ -365,8 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   const int nsplit_gu = min(4, HC / max(2, 1 << LCPG)), nsplit_d = min(4, IC / max(2, 1 << LCPG));
   const bool dswz = I / 2 >= 128;
   const int ncbd = dswz ? I / 256 : 1;
-  const TileGeom geo_gu{16u * 128u, 128u, true};
-  const TileGeom geo_d{dswz ? 16u * 128u : 0u, dswz ? 128u : (uint32_t)(I / 2), dswz};
+  // gate/up tiles: two units of 8 rows, each one TMA box [column block][row][128 B]
+  const TileGeom geo_gu{1024u, 128u, (uint32_t)NCB * 1024u, true};
+  // down tiles: one box of 16 rows, [column block][row][128 B] (or whole rows)
+  const uint32_t pitch_d = dswz ? 128u : (uint32_t)(I / 2);
+  const TileGeom geo_d{16u * pitch_d, pitch_d, 8u * pitch_d, dswz};
   uint64_t pr_lo;
   uint32_t pr_len;  // window of this CTA's prior entries
   align16((uint64_t)re0 * 4, (uint64_t)re1 * 4, pr_lo, pr_len);
@@ -389,13 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     if (b_rw) ptx::bulk_g2s(pa + a.sm.a_rw, G.router_w + (size_t)re0 * H, b_rw, &mbar[0]);
     ptx::bulk_g2s(pa + a.sm.a_wsg, G.shared_gate_w, H * 2, &mbar[0]);
     if (b_nw) ptx::bulk_g2s(pa + a.sm.a_nw, G.norm_w, b_nw, &mbar[0]);
-    for (int u = 0; u < nsu; ++u) {
-      // unit u -> half (u & 1) of tile u / 2; column block cb at cb * 2 KB
-      uint8_t* dst = pa + a.sm.a_sq + (size_t)(u >> 1) * NCB * 2048 + (size_t)(u & 1) * 1024;
-      for (int cb = 0; cb < NCB; ++cb)
-        ptx::tma_load_2d(dst + (size_t)cb * 2048, &a.layers[ll].map_sgu, cb * 128, 8 * (su0 + u),
-                         &mbar[0]);
-    }
+#pragma unroll 1
+    for (int u = 0; u < nsu; ++u)  // unit u is half (u & 1) of tile u / 2
+      ptx::tma_load_4d(pa + a.sm.a_sq + (size_t)u * NCB * 1024, &a.layers[ll].map_sgu, 0,
+                       8 * (su0 + u), 0, 0, &mbar[0]);
     if (b_ssb)
       ptx::bulk_g2s(pa + a.sm.a_ssb, G.shared_blob + G.gu_sb + (size_t)su0 * 32 * HG, b_ssb,
                     &mbar[0]);
@@ -406,22 +396,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     const DecLayer& G = a.layers[ll];
     uint8_t* pb = sm + a.sm.pb + (uint32_t)b * a.sm.pb_bytes;
     const uint32_t b_desc = (uint32_t)sizeof(DecLayer);
-    const uint32_t b_sd = has_down ? (uint32_t)ncbd * 16 * geo_d.pitch : 0;
+    const uint32_t b_sd = has_down ? (uint32_t)ncbd * 16 * pitch_d : 0;
     const uint32_t b_sdsb = has_down ? 16u * IG * 4 : 0;
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive_expect_tx(&mbar[1 + b], b_desc + b_sd + b_sdsb);
     ptx::bulk_g2s(pb + a.sm.b_desc, a.layers + ll, b_desc, &mbar[1 + b]);
     if (has_down) {
-      for (int cb = 0; cb < ncbd; ++cb)
-        ptx::tma_load_2d(pb + a.sm.b_sd + (size_t)cb * geo_d.cb_stride, &a.layers[ll].map_sd,
-                         cb * 128, r0, &mbar[1 + b]);
+      ptx::tma_load_4d(pb + a.sm.b_sd, &a.layers[ll].map_sd, 0, r0, 0, 0, &mbar[1 + b]);
       ptx::bulk_g2s(pb + a.sm.b_sdsb, G.shared_blob + G.d_sb + (size_t)r0 * IG * 4, b_sdsb,
                     &mbar[1 + b]);
     }
   };
 
 #ifdef MOE_DECODE_STAMPS
-  if (a.stamps && tid == 0) a.stamps[(size_t)c * 16 + 15] = ptx::globaltimer_ns();  // kernel entry
+  if (a.stamps && tid == 0) a.stamps[(size_t)c * 32 + 31] = clock64();  // kernel entry
 #endif
   if (tid == 0) {
     for (int i = 0; i < kNumMbar; ++i) ptx::mbar_init(&mbar[i], 1);
@@ -539,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
       ssq = warp_sum(ssq);
       if (lane == 0) s_red[24 + warp] = ssq;
     }
+    if (c == 0 && a.xn_out)  // the block input, for callers that check each layer
+      for (int w = tid; w < XW; w += kThreads)
+        reinterpret_cast<uint32_t*>(a.xn_out + (size_t)l * H)[w] = s_n[w];
     __syncthreads();
     STAMP(1);
 
@@ -561,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (lane == 0) s_part[t] = acc;
       }
     }
+    STAMP(25);
     __syncthreads();
     if (tid <= nr) {
       // the slices pairwise, then the prior
@@ -700,6 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
     __syncthreads();
     STAMP(14);
+    int* s_ok = reinterpret_cast<int*>(sm + a.sm.misc + 816);      // fast path certified
+    float* s_beta = reinterpret_cast<float*>(sm + a.sm.misc + 820);  // the uniform bound
     if (warp == 0) {
       const int nc = (int)s_hist[kBins];
       // uniform bound on every logit's rounding error: 2 D u (|x|_2 max_e |Wr_e|_2
@@ -724,14 +718,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           }
         }
         __syncwarp();
+        STAMP(21);
         // certified when consecutive computed values are more than 2 beta
         // apart over the first `need` positions
         const bool gap = lane + 1 >= need || (s_sval[lane] - s_sval[lane + 1] > 2.0f * beta);
         ok = __all_sync(0xffffffffu, gap);
       }
-      if (!ok)
-        select_exact<8 * V1>(s_log, beta, E, k, reinterpret_cast<const uint16_t*>(s_n),
-                             D.router_w, D.prior, H, sm + a.sm.gu, s_sidx, s_sval);
+      if (lane == 0) {
+        *s_ok = ok ? 1 : 0;
+        *s_beta = beta;
+      }
+      STAMP(22);
+    }
+    __syncthreads();
+    if (!*s_ok) {
+      // near-ties or an overfull candidate set: the exact selection by the
+      // whole CTA (rare)
+      int* si;
+      float* sv;
+      const size_t sel = (rt::topk_warp_smem(E) + 15) & ~size_t(15);
+      // the block input is read from this CTA's shared copy (generic loads)
+      topk_select_block<V1>(SmemLogits{s_log, *s_beta}, E, k, reinterpret_cast<const uint16_t*>(s_n),
+                            D.router_w, D.prior, H, sm + a.sm.gu,
+                            reinterpret_cast<uint2*>(sm + a.sm.gu + sel),
+                            reinterpret_cast<float*>(sm + a.sm.gu + sel + kThreads * V1 * 8), &si,
+                            &sv);
+      if (warp == 0) {
+        if (lane < k) {
+          s_sidx[lane] = si[lane];
+          s_sval[lane] = sv[lane];
+        }
+        __syncwarp();
+      }
+    }
+    if (warp == 0) {
       const float w = renormalised_weight(s_sval, k);
       if (lane < k) {
         const int e = s_sidx[lane];
@@ -746,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           a.topk_w[(size_t)l * k + lane] = w;
         }
       }
+      STAMP(23);
     }
     __syncthreads();
     STAMP(3);
@@ -759,22 +780,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     {
       const DecLayer* Dg = a.layers + l;  // the tensor maps are read from global memory
       if (lane == 0) {
+#pragma unroll 1
         for (int t = warp; t < ntile; t += kWarps) {
           uint32_t bytes = 0;
+#pragma unroll 1
           for (int u = 2 * t; u < min(2 * t + 2, nunit); ++u) {
             const int j = udiv((uint32_t)(4 * (U0 + u)), a.inv_i);
             if (s_slot[j] >= 0) bytes += NCB * 1024 + 32 * HG;
           }
           ptx::fence_proxy_async_smem();
           ptx::mbar_arrive_expect_tx(&mbar[kMbarTile0 + t], bytes);
+#pragma unroll 1
           for (int u = 2 * t; u < min(2 * t + 2, nunit); ++u) {
             const int pg = 4 * (U0 + u);  // first pair of the unit (flattened over experts)
             const int j = udiv((uint32_t)pg, a.inv_i), i = pg - j * I;
             if (s_slot[j] < 0) continue;
-            uint8_t* dst = sm + a.sm.gu + (size_t)t * NCB * 2048 + (size_t)(u & 1) * 1024;
-            for (int cb = 0; cb < NCB; ++cb)
-              ptx::tma_load_3d(dst + (size_t)cb * 2048, &Dg->map_gu, cb * 128, 2 * i, s_slot[j],
-                               &mbar[kMbarTile0 + t]);
+            ptx::tma_load_4d(sm + a.sm.gu + (size_t)u * NCB * 1024, &Dg->map_gu, 0, 2 * i, 0,
+                             s_slot[j], &mbar[kMbarTile0 + t]);
             ptx::bulk_g2s(sm + a.sm.gu_sb + (size_t)u * 32 * HG,
                           D.pool + (uint64_t)s_slot[j] * D.stride + D.gu_sb + (size_t)i * 8 * HG,
                           32u * HG, &mbar[kMbarTile0 + t]);
@@ -786,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           uint32_t bytes = 0;
           if (has_down)
             for (int j = 0; j < k; ++j)
-              if (s_slot[j] >= 0) bytes += (uint32_t)ncbd * 16 * geo_d.pitch + 16u * IG * 4;
+              if (s_slot[j] >= 0) bytes += (uint32_t)ncbd * 16 * pitch_d + 16u * IG * 4;
           ptx::mbar_arrive_expect_tx(&mbar[kMbarDown], bytes);
         }
         __syncwarp();
@@ -795,9 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           for (int j = lane - 1; j >= 0 && j < k; j += 31) {
             if (s_slot[j] < 0) continue;
             uint8_t* dst = sm + a.sm.dn + (size_t)j * a.sm.dn_expert;
-            for (int cb = 0; cb < ncbd; ++cb)
-              ptx::tma_load_3d(dst + (size_t)cb * geo_d.cb_stride, &Dg->map_d, cb * 128, r0,
-                               s_slot[j], &mbar[kMbarDown]);
+            ptx::tma_load_4d(dst, &Dg->map_d, 0, r0, 0, s_slot[j], &mbar[kMbarDown]);
             ptx::bulk_g2s(dst + a.sm.dn_sb,
                           D.pool + (uint64_t)s_slot[j] * D.stride + D.d_sb + (size_t)r0 * IG * 4,
                           16u * IG * 4, &mbar[kMbarDown]);
@@ -838,6 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           s_pgu[t * 16 + g4] = o0;
           s_pgu[t * 16 + g4 + 8] = o1;
         }
+        if (t == 0) STAMP(24);
       }
       STAMP(9);
       __syncthreads();
@@ -866,28 +887,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
       uint8_t* hp_lo = hp_hi + (size_t)NE * 16;
       float* hg = reinterpret_cast<float*>(hp_lo + (size_t)NE * 16);
       const float4* h4 = reinterpret_cast<const float4*>(a.ws.ht);
-      for (int e0 = 0; e0 < NE; e0 += kThreads) {
-        const int e = e0 + tid;
-        float s8 = 0.f;
-        if (e < NE) {
-          const float4 u = __ldcg(h4 + 2 * e), v = __ldcg(h4 + 2 * e + 1);
-          const float f[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-          uint32_t hi[8], lo[8];
+      constexpr int HB = 4;  // entries per thread whose loads are issued together
+      for (int e0 = 0; e0 < NE; e0 += HB * kThreads) {
+        float4 hu[HB], hv[HB];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            hi[q] = f32_to_bf16_rne(f[q]);
-            lo[q] = f32_to_bf16_rne(f[q] - __uint_as_float(hi[q] << 16));
-            s8 += __uint_as_float(hi[q] << 16) + __uint_as_float(lo[q] << 16);
+        for (int q = 0; q < HB; ++q) {
+          const int e = e0 + q * kThreads + tid;
+          if (e < NE) {
+            hu[q] = __ldcg(h4 + 2 * e);
+            hv[q] = __ldcg(h4 + 2 * e + 1);
           }
-          reinterpret_cast<uint4*>(hp_hi)[e] =
-              make_uint4(hi[0] | (hi[4] << 16), hi[1] | (hi[5] << 16), hi[2] | (hi[6] << 16),
-                         hi[3] | (hi[7] << 16));
-          reinterpret_cast<uint4*>(hp_lo)[e] =
-              make_uint4(lo[0] | (lo[4] << 16), lo[1] | (lo[5] << 16), lo[2] | (lo[6] << 16),
-                         lo[3] | (lo[7] << 16));
         }
-        for (int o = 1; o < (a.G >> 3); o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
-        if (e < NE && (e & ((a.G >> 3) - 1)) == 0) hg[e >> (lg - 3)] = s8;
+#pragma unroll
+        for (int q = 0; q < HB; ++q) {
+          const int e = e0 + q * kThreads + tid;
+          float s8 = 0.f;
+          if (e < NE) {
+            const float f[8] = {hu[q].x, hu[q].y, hu[q].z, hu[q].w,
+                                hv[q].x, hv[q].y, hv[q].z, hv[q].w};
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              hi[i] = f32_to_bf16_rne(f[i]);
+              lo[i] = f32_to_bf16_rne(f[i] - __uint_as_float(hi[i] << 16));
+              s8 += __uint_as_float(hi[i] << 16) + __uint_as_float(lo[i] << 16);
+            }
+            reinterpret_cast<uint4*>(hp_hi)[e] =
+                make_uint4(hi[0] | (hi[4] << 16), hi[1] | (hi[5] << 16), hi[2] | (hi[6] << 16),
+                           hi[3] | (hi[7] << 16));
+            reinterpret_cast<uint4*>(hp_lo)[e] =
+                make_uint4(lo[0] | (lo[4] << 16), lo[1] | (lo[5] << 16), lo[2] | (lo[6] << 16),
+                           lo[3] | (lo[7] << 16));
+          }
+          // group sums: the G/8 entries of a group sit on consecutive lanes
+          for (int o = 1; o < (a.G >> 3); o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
+          if (e < NE && (e & ((a.G >> 3) - 1)) == 0) hg[e >> (lg - 3)] = s8;
+        }
       }
       __syncthreads();
       STAMP(5);
@@ -913,7 +948,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           s_pdn[t * 16 + g4] = o0;
           s_pdn[t * 16 + g4 + 8] = o1;
         }
+        if (t == 0) STAMP(20);
       }
+      STAMP(16);
       __syncthreads();
       STAMP(11);
       // y rows in a fixed order: routed experts by rank, then the shared one
@@ -946,13 +983,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
           else if (a.x_out)
             reinterpret_cast<uint32_t*>(a.x_out)[wpos] = nb;
         }
+        STAMP(17);
       }
     } else {
       wait_mbar(&mbar[kMbarDown], par, a.err);  // its phase completes with no bytes
     }
     if (a.chain && l + 1 < L) xarrive(a.ws.cnt + 2 * 16);
+    STAMP(18);
     // the next layer's prologue B into the other buffer (last read two layers ago)
     __syncthreads();
+    STAMP(19);
     if (tid == 0 && l + 1 < L) issue_pro_b(l + 1, b ^ 1);
     STAMP(6);
   }
@@ -1041,7 +1081,7 @@ bool plan_smem(const Dims& d, int nC, bool chain, DecSmem& s) {
   // exact fallback's scratch
   const uint64_t gu_bytes = (uint64_t)tiles_max * NCB * 2048;
   const uint64_t h_bytes = (uint64_t)(k + 1) * I / 8 * 32 + (uint64_t)(k + 1) * IG * 4;
-  const uint64_t sel_bytes = rt::topk_warp_smem(E);
+  const uint64_t sel_bytes = up_to(rt::topk_warp_smem(E), 16) + (uint64_t)kThreads * (kMaxE / 256) * 8 + 64;
   s.gu = take(std::max(gu_bytes, std::max(h_bytes, sel_bytes)), 1024);
   s.gu_sb = take((uint64_t)un_max * 32 * HG, 128);
   s.dn_sb = (uint32_t)up_to((uint64_t)ncbd * 16 * pitch_d, 128);
@@ -1075,11 +1115,12 @@ cudaError_t launch_t(const DecArgs& a, int nC, cudaStream_t st, bool coop) {
 
 template <int NJ, int LC>
 cudaError_t prepare_t(int smem, int* occ) {
+  // the attribute is the kernel's, shared by every context and stack: set
+  // the device limit, so that a smaller plan never lowers it below a larger one
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NJ, LC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<NJ, LC>, kThreads,
-                                                       smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<NJ, LC>, kThreads, smem);
 }
 
 template <int NJ, int LC>
@@ -1147,20 +1188,27 @@ __global__ void router_bound_consts_kernel(const uint16_t* __restrict__ rw,
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-// A TMA map over packed-code rows of `row_bytes` bytes: {row_bytes, rows,
-// slots} (slots > 1: 3-D), box {min(128, row_bytes), box_rows, 1}, the
-// 128-byte swizzle when a row holds 128 bytes or more.
+// A 4-D TMA map over packed-code rows of `row_bytes` bytes, ordered so that
+// one box lands as [column block][row][128 B]: dims {bytes within a 128-byte
+// column block, row, column block, slot} with strides {row_bytes, 128,
+// slot_stride}; box {128, box_rows, all column blocks, 1}, the 128-byte
+// swizzle.  Rows shorter than 128 bytes are one unswizzled column block.
 bool encode_rows(CUtensorMap* m, const uint8_t* base, int row_bytes, int rows, int slots,
                  uint64_t slot_stride, int box_rows) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const bool swz = row_bytes >= 128;
-  const cuuint64_t dim[3] = {(cuuint64_t)row_bytes, (cuuint64_t)rows, (cuuint64_t)slots};
-  const cuuint64_t stride[2] = {(cuuint64_t)row_bytes, (cuuint64_t)slot_stride};
-  const cuuint32_t box[3] = {swz ? 128u : (cuuint32_t)row_bytes, (cuuint32_t)box_rows, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, slots > 1 ? 3 : 2, const_cast<uint8_t*>(base), dim,
-             stride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const cuuint64_t inner = swz ? 128u : (cuuint64_t)row_bytes;
+  const cuuint64_t ncb = (cuuint64_t)row_bytes / inner;
+  // a single slot still needs a valid stride (a multiple of 16 bytes)
+  const cuuint64_t sstride =
+      slots > 1 ? (cuuint64_t)slot_stride : ((cuuint64_t)rows * row_bytes + 15) / 16 * 16;
+  const cuuint64_t dim[4] = {inner, (cuuint64_t)rows, ncb, (cuuint64_t)slots};
+  const cuuint64_t stride[3] = {(cuuint64_t)row_bytes, inner, sstride};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)box_rows, (cuuint32_t)ncb, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dim, stride, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1221,6 +1269,11 @@ void decode_workspace_carve(const Dims& d, int nC, uint8_t* base, DecWorkspace* 
   w->xt = reinterpret_cast<uint16_t*>(base + off);
 }
 
+void decode_workspace_reset(int nC, const DecWorkspace& w) {
+  cudaMemset(w.seq, 0, (size_t)nC * 4);
+  cudaMemset(w.cnt, 0, 3 * 16 * 8);
+}
+
 cudaError_t decode_launch(const Dims& d, int nC, const DecLaunch& p, cudaStream_t st) {
   DecArgs a{};
   a.layers = p.layers;
@@ -1232,6 +1285,7 @@ cudaError_t decode_launch(const Dims& d, int nC, const DecLaunch& p, cudaStream_
   a.x = p.x;
   a.x_out = p.x_out;
   a.y = p.y;
+  a.xn_out = p.xn_out;
   a.topk_idx = p.topk_idx;
   a.topk_w = p.topk_w;
   a.perm = p.perm;

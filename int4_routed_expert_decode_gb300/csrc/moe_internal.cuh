@@ -18,8 +18,8 @@ constexpr int kSyncWords = 1;  // counters of the fused decode kernel
 inline bool hidden_supported(int H) {
   return H >= 256 && H <= kMaxH && H % 256 == 0 && ((H / 256) & (H / 256 - 1)) == 0;
 }
-constexpr int kTileRouterMinT = 16;
-constexpr int kPathFusedV1 = 4;  // the earlier barrier-based fused decode kernel (comparison)  // from this many tokens the router is a tiled GEMM
+constexpr int kTileRouterMinT = 16;  // from this many tokens the router is a tiled GEMM
+constexpr int kPathFusedV1 = 4;  // the earlier barrier-based fused decode kernel (comparison)
 // Floats of the router's slice sums: the slices are only used while
 // slices x tiles <= 2 x SMs, and a tile covers 64 x 128 logits.
 inline int64_t tile_router_part_floats(int num_sms) { return (int64_t)2 * num_sms * 64 * 128; }
@@ -52,10 +52,11 @@ EncodeTiledFn encode_tiled();
 // Per-layer resident weights and constants, read by the kernel from device
 // memory (and copied into shared memory with each layer's prologue).
 struct alignas(64) DecLayer {
-  // TMA maps of the packed codes (rows of 128-byte column blocks, 128-byte
-  // swizzle where a row holds at least 128 bytes): routed gate/up
-  // {H/2 bytes, 2I rows, slots} box {128, 8, 1}; routed down {I/2, H, slots}
-  // box {min(128, I/2), 16, 1}; the shared expert's the same with one slot
+  // 4-D TMA maps of the packed codes {bytes of a 128-byte column block, row,
+  // column block, slot} (128-byte swizzle; rows under 128 bytes are one
+  // unswizzled block), one box per copy landing as [column block][row][bytes]:
+  // routed gate/up 2I rows of H/2 bytes, box 8 rows; routed down H rows of
+  // I/2 bytes, box 16 rows; the shared expert's the same with one slot
   CUtensorMap map_gu, map_d, map_sgu, map_sd;
   const uint16_t* router_w;       // [E][H]
   const float* prior;             // [E] or null
@@ -176,6 +177,7 @@ struct DecLaunch {
   const uint16_t* x;
   uint16_t* x_out;
   uint16_t* y;
+  uint16_t* xn_out;  // [L][H] block inputs (after the RMSNorm), or null
   int32_t* topk_idx;
   float* topk_w;
   int32_t* perm;
@@ -194,6 +196,8 @@ bool decode_fits(const Dims& d, int nC, bool chain);
 cudaError_t decode_prepare(const Dims& d, int nC, bool chain, int* ok);
 size_t decode_workspace_bytes(const Dims& d, int nC);
 void decode_workspace_carve(const Dims& d, int nC, uint8_t* base, DecWorkspace* w);
+// Zero the launch and arrival counters (synchronous; nothing may be in flight).
+void decode_workspace_reset(int nC, const DecWorkspace& w);
 cudaError_t decode_router_consts(const uint16_t* router_w, const float* prior, int E, int H,
                                  float* out, cudaStream_t st);
 // The four TMA maps of a layer's descriptor (host-side encoding).

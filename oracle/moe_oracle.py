@@ -279,3 +279,67 @@ def moe_block(x_bits: np.ndarray, W: dict, k: int, group: int, tokens=None) -> d
         y[r] = acc + gate[t] * shared[r]
     return {"y": y, "topk_idx": idx, "topk_w": wts, "shared_gate": gate, "perm": perm,
             "offsets": offsets, "logits": logits, "tokens": toks}
+
+
+# ----------------------------------------------------------------------------
+# a stack of blocks for one token: RMSNorm in, residual out
+# ----------------------------------------------------------------------------
+# The pages run the blocks one decoder layer after another (README "Status":
+# the decode loop is dispatch bound) but print no equations for what sits
+# between them.  Reading: the plain pre-norm residual form of the Qwen3-Next
+# decoder, without the attention sub-layer: n = RMSNorm(x) * norm_w,
+# x <- x + MoE(n); every tensor passed between steps is bf16.
+def f64_to_bf16_bits(v) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even); uint16 bit patterns.
+
+    A finite v = m * 2^e with 1/2 <= |m| < 1 keeps 8 significant bits:
+    rint(m * 2^8) * 2^(e - 8), rint rounding half to even.  Values here are
+    far from bf16's overflow and underflow, which are not handled.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)  # exact in float64 and in float32
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def rms_norm(x_bits, norm_w_bits, eps: float) -> np.ndarray:
+    """bf16 bits of x / sqrt(mean_h x_h^2 + eps) * g (float64, rounded once).
+
+    g = norm_w (bf16) or all ones when norm_w_bits is None.
+    """
+    x = bf16_to_f64(x_bits)
+    g = np.ones_like(x) if norm_w_bits is None else bf16_to_f64(norm_w_bits)
+    r = 1.0 / math.sqrt(float(np.mean(x * x)) + eps)
+    return f64_to_bf16_bits(x * r * g)
+
+
+def residual_add(x_bits, y) -> np.ndarray:
+    """bf16 bits of x + bf16(y): the block output is rounded to bf16 first."""
+    yb = f64_to_bf16_bits(y)
+    return f64_to_bf16_bits(bf16_to_f64(x_bits) + bf16_to_f64(yb))
+
+
+def moe_stack(x_bits, Ws: list, norm_ws, k: int, group: int, eps: float, xn_given=None) -> dict:
+    """One token through len(Ws) blocks.
+
+    For l = 0, 1, ...: n_l = rms_norm(x_l), block l on n_l, x_{l+1} =
+    residual_add(x_l, y_l).  ``xn_given`` (optional [L][H] bf16 bits)
+    replaces each n_l, so that each block can be checked on exactly the input
+    another implementation used.  Returns x (inputs, [L+1][H] bits, last =
+    the result), xn [L][H] bits, y float64 [L][H], topk_idx [L][k], topk_w.
+    """
+    x = np.asarray(x_bits, dtype=np.uint16).reshape(-1)
+    L = len(Ws)
+    xs, xns, ys, idxs, wts = [x], [], [], [], []
+    for l in range(L):
+        g = None if norm_ws is None else norm_ws[l]
+        n = rms_norm(x, g, eps) if xn_given is None else np.asarray(xn_given[l], np.uint16)
+        r = moe_block(n[None, :], Ws[l], k, group)
+        x = residual_add(x, r["y"][0])
+        xns.append(n)
+        ys.append(r["y"][0])
+        idxs.append(r["topk_idx"][0])
+        wts.append(r["topk_w"][0])
+        xs.append(x)
+    return {"x": np.stack(xs), "xn": np.stack(xns), "y": np.stack(ys),
+            "topk_idx": np.stack(idxs), "topk_w": np.stack(wts)}

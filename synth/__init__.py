@@ -169,6 +169,14 @@ def layer_weights(seed: int, workload: int, layer: int, shape: Shape,
     }
 
 
+T_NORM_W = 30  # tensor id of the stacks' RMSNorm weights (ids below 30 are the C generator's)
+
+
+def norm_weights(seed: int, workload: int, layer: int, H: int) -> np.ndarray:
+    """RMSNorm weights of one layer of a stack, bf16 [H] ~ N(1, 0.1^2)."""
+    return normal_bf16(stream_key(seed, workload, layer, T_NORM_W, 0), H, 1.0, 0.1)
+
+
 def tokens(seed: int, workload: int, layer: int, step: int, T: int, H: int) -> np.ndarray:
     """Token activations bf16 [T, H] ~ N(0,1) for one (layer, step)."""
     x = np.empty((T, H), np.uint16)

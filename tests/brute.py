@@ -97,3 +97,47 @@ def block(x_bits, W: dict, k: int, group: int) -> dict:
     offsets = [sum(1 for e in flat if e < b) for b in range(E + 1)]
     return {"y": ys, "topk_idx": idxs, "topk_w": wss, "gate": gates, "perm": perm,
             "offsets": offsets}
+
+
+def bf16_round(v: float) -> int:
+    """bf16 bits of float v, nearest with ties to even, from the float64 bit
+    fields (integer arithmetic only)."""
+    u = struct.unpack(">Q", struct.pack(">d", float(v)))[0]
+    sign, exp, frac = u >> 63, (u >> 52) & 0x7FF, u & ((1 << 52) - 1)
+    if exp == 0 and frac == 0:
+        return sign << 15
+    mant = (1 << 52) | frac            # 53 significant bits, value mant * 2^(exp - 1075)
+    keep, drop = mant >> 45, mant & ((1 << 45) - 1)  # 8 bits kept
+    half = 1 << 44
+    if drop > half or (drop == half and keep & 1):
+        keep += 1
+    if keep == 1 << 8:                 # carried into a new binade
+        keep >>= 1
+        exp += 1
+    e32 = exp - 1023 + 127             # float32 exponent field
+    assert 0 < e32 < 255, v
+    return (sign << 15) | (e32 << 7) | (keep & 0x7F)
+
+
+def rms_norm(x_bits, g_bits, eps: float) -> list:
+    x = [bf16(b) for b in x_bits]
+    g = [1.0] * len(x) if g_bits is None else [bf16(b) for b in g_bits]
+    ms = math.fsum(v * v for v in x) / len(x)
+    d = math.sqrt(ms + eps)
+    return [bf16_round(x[h] / d * g[h]) for h in range(len(x))]
+
+
+def stack(x_bits, Ws: list, norm_ws, k: int, group: int, eps: float) -> dict:
+    """One token through the blocks: n = rms_norm(x), x <- bf16(x + bf16(y))."""
+    x = [int(b) for b in x_bits]
+    out = {"x": [x], "xn": [], "y": [], "topk_idx": []}
+    for l, W in enumerate(Ws):
+        n = rms_norm(x, None if norm_ws is None else norm_ws[l], eps)
+        r = block([n], W, k, group)
+        y = r["y"][0]
+        x = [bf16_round(bf16(x[h]) + bf16(bf16_round(y[h]))) for h in range(len(x))]
+        out["xn"].append(n)
+        out["y"].append(y)
+        out["topk_idx"].append(r["topk_idx"][0])
+        out["x"].append(x)
+    return out

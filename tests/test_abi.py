@@ -78,3 +78,16 @@ def test_static_routing_rejects_uninstantiated_hidden_up_front(L, hidden):
     rc = L.moe_route_static(None, 1, None, None, None, 16, 2, hidden, None, None, None, None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
     assert "hidden" in moe.moe_last_error(None)
+
+
+def test_stack_calls_reject_null_arguments(L):
+    out = ctypes.c_void_p()
+    assert L.moe_stack_create(None, 2, None, ctypes.c_float(1e-6), ctypes.byref(out)) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert "layers" in moe.moe_last_error(None)
+    assert L.moe_stack_create(None, 0, None, ctypes.c_float(1e-6), None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_forward(None, None, None, None, None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_get_status(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_set_test_flags(None, 0) == moe.MOE_ERR_INVALID_ARG
+    L.moe_stack_destroy(None)

@@ -17,7 +17,10 @@ PINS = [
     P.test_block_matches_pure_python_brute_force, P.test_block_with_prior_matches_brute_force,
     P.test_dense_mixture_at_k_equals_E, P.test_identical_experts_reduce_to_one,
     P.test_zero_routed_experts_leave_the_shared_term, P.test_down_projection_is_linear_in_its_scales,
-    P.test_hand_worked_block,
+    P.test_hand_worked_block, P.test_bf16_rounding_hand_worked, P.test_rms_norm_hand_worked,
+    P.test_rms_norm_invariants, P.test_residual_rounds_the_block_output_first,
+    P.test_stack_of_zero_blocks_keeps_the_residual, P.test_stack_matches_pure_python_brute_force,
+    P.test_stack_closed_form_layer,
 ]
 
 
@@ -83,7 +86,31 @@ def _sigmoid_gate_dropped(z):
     return np.ones_like(np.asarray(z, dtype=np.float64))
 
 
+def _bf16_truncate(v):
+    v = np.asarray(v, dtype=np.float64)
+    return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _rms_norm_sum(x_bits, norm_w_bits, eps):
+    x = O.bf16_to_f64(x_bits)
+    g = np.ones_like(x) if norm_w_bits is None else O.bf16_to_f64(norm_w_bits)
+    return O.f64_to_bf16_bits(x / np.sqrt(np.sum(x * x) + eps) * g)
+
+
+def _rms_norm_no_weight(x_bits, norm_w_bits, eps):
+    return ORIG_RMS(x_bits, None, eps)
+
+
+def _rms_norm_no_eps(x_bits, norm_w_bits, eps):
+    return ORIG_RMS(x_bits, norm_w_bits, 0.0)
+
+
+def _residual_unrounded(x_bits, y):
+    return O.f64_to_bf16_bits(O.bf16_to_f64(x_bits) + np.asarray(y, np.float64))
+
+
 ORIG_ROUTE = O.route
+ORIG_RMS = O.rms_norm
 
 MUTATIONS = {
     "nibble order high-first": ("unpack_int4", _unpack_high_first),
@@ -97,6 +124,11 @@ MUTATIONS = {
     "unstable permutation": ("permutation", _perm_unstable),
     "no renormalisation": ("route", _route_no_renorm),
     "shared gate dropped": ("sigmoid", _sigmoid_gate_dropped),
+    "bf16 by truncation": ("f64_to_bf16_bits", _bf16_truncate),
+    "rms over the sum, not the mean": ("rms_norm", _rms_norm_sum),
+    "norm weight ignored": ("rms_norm", _rms_norm_no_weight),
+    "norm eps dropped": ("rms_norm", _rms_norm_no_eps),
+    "residual adds y unrounded": ("residual_add", _residual_unrounded),
 }
 
 

@@ -353,3 +353,105 @@ def _hand_worked_inputs(g):
          "experts": stacked, "shared": shared}
     x = np.array([[_bf16_bits(v) for v in row] for row in g["x"]], np.uint16)
     return W, x, g["k"], group
+
+
+# --------------------------------------------------------------------------- stacks
+def test_bf16_rounding_hand_worked():
+    """Nearest with ties to even, worked by hand: 1 + 2^-8 is halfway between 1
+    and 1 + 2^-7 (even: 1); 1 + 3*2^-8 halfway between 1 + 2^-7 and 1 + 2^-6
+    (even: 1 + 2^-6); a hair above a tie rounds up.  Catches truncation and
+    ties away from zero."""
+    vals = [1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -2.5, 1 + 2 ** -8 + 2 ** -20, -(1 + 2 ** -8)]
+    want = [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x3F81, 0xBF80]
+    assert O.f64_to_bf16_bits(np.array(vals)).tolist() == want
+    assert [brute.bf16_round(v) for v in vals] == want
+
+
+def test_rms_norm_hand_worked():
+    """x = (3, 4): mean of squares 12.5, x / sqrt(12.5) = (0.84853, 1.13137),
+    in bf16 217/256 = 0.84765625 (0x3F59) and 2 * 145/256 = 1.1328125 (0x3F91);
+    with g = (2, 0.5): 1.6953125 (0x3FD9) and 0.56640625 (0x3F11)."""
+    x = np.array([_bf16_bits(3.0), _bf16_bits(4.0)], np.uint16)
+    assert O.rms_norm(x, None, 1e-30).tolist() == [0x3F59, 0x3F91]
+    g = np.array([_bf16_bits(2.0), _bf16_bits(0.5)], np.uint16)
+    assert O.rms_norm(x, g, 1e-30).tolist() == [0x3FD9, 0x3F11]
+
+
+def test_rms_norm_invariants():
+    """Scaling x by a power of two changes nothing (eps negligible); with unit
+    weights the mean square of the output is 1 up to bf16 rounding; eps
+    dominates a tiny input: n = x / sqrt(eps)."""
+    H = 512
+    x = _x(1, H, layer=4)[0]
+    n = O.rms_norm(x, None, 1e-30)
+    x4 = O.f64_to_bf16_bits(O.bf16_to_f64(x) * 4.0)
+    assert np.array_equal(O.rms_norm(x4, None, 1e-30), n)
+    ms = float(np.mean(O.bf16_to_f64(n) ** 2))
+    assert abs(ms - 1.0) < 2 ** -7
+    tiny = O.f64_to_bf16_bits(O.bf16_to_f64(x) * 2.0 ** -40)
+    got = O.bf16_to_f64(O.rms_norm(tiny, None, 1.0))
+    assert np.allclose(got, O.bf16_to_f64(tiny), rtol=2 ** -7, atol=0)
+
+
+def test_residual_rounds_the_block_output_first():
+    """x = 1, y = 2^-8 + 2^-20: bf16(y) = 2^-8 and 1 + 2^-8 is a tie that goes
+    to 1 (even); adding y unrounded would give 1 + 2^-7."""
+    x = np.array([_bf16_bits(1.0)], np.uint16)
+    assert O.residual_add(x, np.array([2 ** -8 + 2 ** -20])).tolist() == [0x3F80]
+    assert O.residual_add(x, np.array([3 * 2 ** -8])).tolist() == [0x3F82]
+
+
+def test_stack_of_zero_blocks_keeps_the_residual():
+    """All expert and shared weights zero: every block outputs 0 and x passes
+    through every layer unchanged, whatever the norm weights."""
+    W = _tiny_weights(layer=2)
+    for part in ("experts", "shared"):
+        for m in ("gate", "up", "down"):
+            W[part][m + "_q"] = np.zeros_like(W[part][m + "_q"])
+            W[part][m + "_b"] = np.zeros_like(W[part][m + "_b"])
+    x = _x(1, TINY.H, layer=2)[0]
+    g = [O.f64_to_bf16_bits(np.full(TINY.H, 1.5))] * 3
+    out = O.moe_stack(x, [W] * 3, g, TINY.k, TINY.G, 1e-6)
+    assert np.all(out["y"] == 0.0)
+    for l in range(4):
+        assert np.array_equal(out["x"][l], x)
+
+
+def test_stack_matches_pure_python_brute_force():
+    """Three tiny layers with their own weights and norm weights against the
+    pure-Python restatement (integer bf16 rounding, fsum, exact logits)."""
+    Ws = [_tiny_weights(layer=10 + l) for l in range(3)]
+    x = _x(1, TINY.H, layer=10)[0]
+    rng = np.random.default_rng(5)
+    g = [O.f64_to_bf16_bits(1.0 + 0.25 * rng.standard_normal(TINY.H)) for _ in range(3)]
+    out = O.moe_stack(x, Ws, g, TINY.k, TINY.G, 1e-6)
+    ref = brute.stack(x.tolist(), [_as_lists(W) for W in Ws], [v.tolist() for v in g],
+                      TINY.k, TINY.G, 1e-6)
+    assert out["topk_idx"].tolist() == ref["topk_idx"]
+    assert out["xn"].tolist() == ref["xn"]
+    assert out["x"].tolist() == ref["x"]
+    y = np.array(ref["y"])
+    assert np.max(np.abs(out["y"] - y)) <= 1e-12 * np.max(np.abs(y))
+
+
+def test_stack_given_inputs_replace_the_norm():
+    """xn_given feeds each block exactly that input (the residual still runs)."""
+    Ws = [_tiny_weights(layer=20 + l) for l in range(2)]
+    x = _x(1, TINY.H, layer=20)[0]
+    xn = _x(2, TINY.H, layer=21)
+    out = O.moe_stack(x, Ws, None, TINY.k, TINY.G, 1e-6, xn_given=xn)
+    for l in range(2):
+        ref = brute.block([xn[l].tolist()], _as_lists(Ws[l]), TINY.k, TINY.G)
+        assert out["topk_idx"][l].tolist() == ref["topk_idx"][0]
+        assert np.array_equal(out["xn"][l], xn[l])
+
+
+def test_stack_closed_form_layer():
+    """The closed-form layer of the C++ oracle's pins (block output 2^-8 + 2^-20,
+    residual tie to even) on the numpy oracle."""
+    from tests.test_oracle_cpp import closed_form_stack_layer
+    W, x = closed_form_stack_layer()
+    out = O.moe_stack(x, [W], None, TINY.k, TINY.G, 1e-6)
+    assert np.all(out["xn"][0] == 0x3F80)
+    assert np.all(out["y"][0] == 2.0 ** -8 + 2.0 ** -20)
+    assert np.all(out["x"][1] == 0x3F80)
