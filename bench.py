@@ -188,30 +188,48 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- oracle timing
-def oracle_units(wl, budget_s, layers, check=None):
-    """Time the CPU oracle on (layer, token) passes of the workload for about
-    budget_s seconds.  Returns (passes/s, passes, seconds, sample text, results)."""
-    from oracle import moe_oracle as O
+def oracle_units(wl, budget_s, layers, stacked, threads=0):
+    """Time the C++ CPU oracle (OpenMP; `threads` 0 = all cores) on (layer,
+    token) passes of the workload for about budget_s seconds.  A stack pass
+    includes the RMSNorm and the residual add.  Returns (passes/s, passes,
+    seconds, sample text)."""
+    from oracle import cpp as C
     n_layers = min(layers, 2)
     Ws = [synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s) for l in range(n_layers)]
+    norms = stack_norm_weights(wl, n_layers)
     tok = 1 if wl.T == 1 else min(wl.T, 8)
-    done, results = 0, []
+    x_state = synth.tokens(0, wl.wid, 0, 0, 1, wl.H)[0]
+    done = 0
+    C.load()  # compile outside the timed region
     t0 = time.perf_counter()
     step = 0
     while True:
         l = step % n_layers
-        x = synth.tokens(0, wl.wid, l, step // n_layers, wl.T, wl.H)
-        rows = list(range(tok))
-        r = O.moe_block(x, Ws[l], wl.k, wl.G, tokens=rows)
-        results.append((l, step // n_layers, rows, r))
+        if stacked:
+            r = C.moe_stack(x_state, [Ws[l]], [norms[l]], wl.k, wl.G, STACK_EPS, threads=threads)
+            x_state = r["x"][1]
+        else:
+            x = synth.tokens(0, wl.wid, l, step // n_layers, wl.T, wl.H)
+            C.moe_block(x, Ws[l], wl.k, wl.G, tokens=list(range(tok)), threads=threads)
         done += tok
         step += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    sample = (f"{done} (layer, token) passes of the CPU oracle over layers 0..{n_layers - 1}, "
-              f"{tok} token(s) per pass" + ("" if wl.T == 1 else f" of a {wl.T}-token batch"))
-    return done / dt, done, dt, sample, results
+    sample = (f"{done} (layer, token) passes of the C++ oracle over layers 0..{n_layers - 1}, "
+              f"{tok} token(s) per pass" + ("" if wl.T == 1 else f" of a {wl.T}-token batch") +
+              (" (RMSNorm and residual included)" if stacked else ""))
+    return done / dt, done, dt, sample
+
+
+def cpu_baseline(wl, budget_s, L, stacked):
+    """The oracle on all host cores, and on one core for a single-thread figure."""
+    v, n, dt, sample = oracle_units(wl, budget_s * 0.7, L, stacked, threads=0)
+    v1, n1, dt1, _ = oracle_units(wl, budget_s * 0.3, L, stacked, threads=1)
+    return {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+            "sample": sample + f", {dt:.1f} s on {cores_used()} threads",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} passes, {dt1:.1f} s"}}
 
 
 def cores_used():
@@ -226,7 +244,7 @@ def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from oracle import moe_oracle as O
+    from oracle import cpp as C
     L = args.layers or wl.layers
     n_layers = min(L, 2)
     Ws = [synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s) for l in range(n_layers)]
@@ -234,16 +252,16 @@ def run_reference(args, wl):
     stacked = stack_mode(args, wl)
     norms = stack_norm_weights(wl, n_layers)
     state = {"x": synth.tokens(0, wl.wid, 0, 0, 1, wl.H)[0]}
+    C.load()  # compiled before timing
 
     def step(i):
         l = i % n_layers
         if stacked:  # one layer of the residual stack: RMSNorm, block, residual add
-            n = O.rms_norm(state["x"], norms[l], STACK_EPS)
-            r = O.moe_block(n[None, :], Ws[l], wl.k, wl.G)
-            state["x"] = O.residual_add(state["x"], r["y"][0])
+            r = C.moe_stack(state["x"], [Ws[l]], [norms[l]], wl.k, wl.G, STACK_EPS)
+            state["x"] = r["x"][1]
             return
         x = synth.tokens(0, wl.wid, l, i // n_layers, wl.T, wl.H)
-        O.moe_block(x, Ws[l], wl.k, wl.G, tokens=list(range(tok)))
+        C.moe_block(x, Ws[l], wl.k, wl.G, tokens=list(range(tok)))
 
     for i in range(args.warmup):
         step(i)
@@ -260,7 +278,8 @@ def run_reference(args, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": config_of(wl, L, stacked),
-        "note": "CPU oracle (numpy float64), a bounded sample of the workload per step",
+        "note": "C++ CPU oracle (float64, OpenMP on all host cores), a bounded sample of the "
+                "workload per step",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -454,22 +473,19 @@ def run_ours(args, wl):
         ms_e2e = e0.elapsed_time(e1) / k_e2e
     e2e_value = world * T * L / (ms_e2e / 1e3)
 
-    # CPU oracle on the host cores (rank 0, N = 1), and a parity spot check
+    # C++ oracle on the host cores (rank 0, N = 1), and a parity spot check of
+    # layer 0's first eager step against the numpy oracle
     cpu = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
-        v, n, dt, sample, results = oracle_units(wl, args.cpu_budget, L)
-        cpu = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
-               "sample": sample + f", {dt:.1f} s"}
-        # results of (layer l, input step s) for s < S can be checked against the eager pass
-        errs = []
-        for (l, s, rows, r) in results:
-            if s == 0:
-                yg = ys0[l, rows].float().cpu().numpy().astype(np.float64)
-                d = np.abs(yg - r["y"])
-                errs.append(float(d.max() / np.abs(r["y"]).max()))
-        if errs:
-            parity = {"checked_passes": len(errs), "max_rel_err": max(errs)}
+        cpu = cpu_baseline(wl, args.cpu_budget, L, False)
+        from oracle import moe_oracle as O
+        W0 = synth.layer_weights(0, wl.wid, 0, wl.shape, zipf_s=wl.zipf_s)
+        rows = list(range(min(T, 4)))
+        r = O.moe_block(synth.tokens(0, wl.wid, 0, 0, T, H), W0, wl.k, wl.G, tokens=rows)
+        yg = ys0[0, rows].float().cpu().numpy().astype(np.float64)
+        parity = {"checked": f"layer 0, rows {rows}",
+                  "max_rel_err": float(np.abs(yg - r["y"]).max() / np.abs(r["y"]).max())}
 
     P = T * wl.k
     flops = {"gateup": 2.0 * H * (2 * wl.I * P + 2 * wl.Is * T),
@@ -643,9 +659,7 @@ def run_ours_stack(args, wl):
     cpu = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
-        v, n, dt, sample, _ = oracle_units(wl, args.cpu_budget, L)
-        cpu = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
-               "sample": sample + f", {dt:.1f} s"}
+        cpu = cpu_baseline(wl, args.cpu_budget, L, True)
         # layers 0 and L-1 of the first step against the oracle on the GPU's block input
         from oracle import moe_oracle as O
         y0, xn0, idx0 = first

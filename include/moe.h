@@ -89,7 +89,8 @@ typedef struct moe_weights {
   moe_qmatrix gate, up, down;
 } moe_weights;
 
-/* Create a context for one MoE layer.
+/* Create a context for one MoE layer (the sparse block of a decoder layer:
+ * routed experts, a resident shared expert; README "How it works").
  *   E in [1, 1024]; k in [1, min(E, 32)]; hidden in {256, 512, 1024, 2048,
  *   4096, 8192}; inter and shared_inter multiples of group, at most 4096;
  *   group in {32, 64, 128}.  Nothing is allocated on the device yet.
@@ -98,8 +99,10 @@ typedef struct moe_weights {
  * no device is current. */
 int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out);
 
-/* Copy and repack the weights into library-owned device memory: the routed
- * experts become n_slots fixed-stride blobs (slot s holds the s-th expert of
+/* Copy and repack the weights into library-owned device memory (the pages'
+ * routed experts live in a container "built from fixed-stride blobs for fast
+ * seeking", README "How it works"; MLX affine int4 layout per the list of
+ * what was built): the routed experts become n_slots fixed-stride blobs (slot s holds the s-th expert of
  * `w`, 64-bit byte offsets), the router, prior, shared gate vector and shared
  * expert stay resident beside them.  Synchronous: when it returns the caller
  * may free or reuse every buffer of `w`.  May be called again to replace the
@@ -108,13 +111,16 @@ int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group,
 int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stream);
 
 /* Size the device workspace for up to max_T tokens per moe_forward call
+ * (the pages have no counterpart: it keeps moe_forward free of allocations)
  * (max_T in [1, 1<<20]).  Must be called before moe_forward and before any
  * CUDA-graph capture of it; moe_forward never allocates.  Synchronous.
  * Errors: INVALID_ARG, OOM. */
 int moe_reserve(moe_ctx* ctx, int max_T);
 
 /* One pass of the block over T tokens, enqueued on `stream` (asynchronous,
- * no host synchronisation, no allocation: capturable in a CUDA graph).
+ * no host synchronisation, no allocation: capturable in a CUDA graph): the
+ * router, top-k, shared expert and routed experts of README "How it works",
+ * with the slot table standing for the pages' bounded expert pool.
  *   x                  bf16 [T][H] device, read only
  *   expert_slot_table  int32 [E] device: slot holding expert e, or NULL for
  *                      the identity (requires n_slots >= E).  A selected
@@ -131,24 +137,40 @@ int moe_reserve(moe_ctx* ctx, int max_T);
  * T = 0 is a no-op.  x and y must not overlap.
  * Errors (host side, nothing launched): INVALID_ARG, NOT_LOADED,
  * NOT_RESERVED (T > max_T), CUDA (launch failure).  Errors found on the
- * device are sticky and reported by moe_get_status. */
+ * device are sticky and reported by moe_get_status.
+ *
+ * Co-residency: for T = 1 the single-launch decode kernels run one CTA per
+ * SM and exchange data between all of them through counters in device
+ * memory.  They are launched without the cooperative attribute (it would
+ * keep each layer from overlapping the previous one's tail, about 2.5 us per
+ * layer), so they need every SM free of other work while they run: a kernel
+ * of another stream, or an MPS client, holding an SM makes the exchange wait
+ * out its bound (about one second), the device records MOE_ERR_TIMEOUT and y
+ * of that call is not valid.  moe_stack_forward launches cooperatively
+ * instead (one launch per token).  The exchange counters only grow and every
+ * launch reads them afresh, so a CUDA graph captured around moe_forward keeps
+ * replaying correctly; moe_get_status zeroes them after a device error. */
 int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_table, void* y,
                 int32_t* topk_idx, float* topk_w, int32_t* perm, int32_t* offsets, void* stream);
 
 /* Synchronise `stream`, then return and clear the sticky device error word
  * (MOE_OK, MOE_ERR_SLOT or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if the
- * synchronisation itself failed. */
+ * synchronisation itself failed.  After a device error it also zeroes the
+ * decode kernels' exchange counters (synchronously; nothing of this context
+ * may be in flight on another stream).  No counterpart on the pages. */
 int moe_get_status(moe_ctx* ctx, void* stream);
 
 /* Read slot `slot` (or the shared expert when slot == -1) back from the
- * device pool into host buffers in the canonical layout of moe_weights
+ * device pool (MLX affine int4, list of what was built) into host buffers in
+ * the canonical layout of moe_weights
  * (gate/up [I][H], down [H][I]; I = shared_inter for the shared expert).
  * Synchronous.  Used to verify the repacking byte for byte. */
 int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, uint16_t* gate_b,
                     uint32_t* up_q, uint16_t* up_s, uint16_t* up_b, uint32_t* down_q,
                     uint16_t* down_s, uint16_t* down_b);
 
-/* Kernel path of moe_forward.  MOE_PATH_AUTO uses the fused single-launch
+/* Kernel path of moe_forward (an implementation choice; the pages run one
+ * Metal shader sequence).  MOE_PATH_AUTO uses the fused single-launch
  * decode kernel for T = 1 when the sizes allow it (hidden in {256, 512,
  * 1024, 2048}, inter == shared_inter <= 1024), the tensor-core grouped GEMMs
  * for T >= 2 when hidden, 2*inter and 2*shared_inter are multiples of 128,
@@ -162,7 +184,8 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
 enum { MOE_PATH_AUTO = 0, MOE_PATH_DECODE = 1, MOE_PATH_GENERAL = 2, MOE_PATH_PREFILL = 3 };
 int moe_set_path(moe_ctx* ctx, int path);
 
-/* Test hooks, off by default.  MOE_TEST_WAIT_TIMEOUT makes the grid
+/* Test hooks, off by default (failure injection on the host side of a
+ * bounded device wait; no counterpart on the pages).  MOE_TEST_WAIT_TIMEOUT makes the grid
  * barriers of the fused decode kernel wait for one arrival more than the
  * grid has, and the MMA issuer of each grouped-GEMM CTA wait on an mbarrier
  * phase that nothing completes: each bounded wait runs out (about one
@@ -200,12 +223,14 @@ enum {
 };
 int moe_set_stage_events(moe_ctx* ctx, void* const* events, int n_events);
 
-/* Bytes of one routed-expert blob (codes + scales + biases, padded) and the
- * number of resident device bytes of the context (weights + workspace). */
+/* Bytes of one routed-expert blob (codes + scales + biases, padded: the
+ * pages' fixed-stride blob, README "How it works") and the number of
+ * resident device bytes of the context (weights + workspace). */
 int64_t moe_expert_blob_bytes(const moe_ctx* ctx);
 int64_t moe_device_bytes(const moe_ctx* ctx);
 
-/* Number of kernel launches the last moe_forward enqueued. */
+/* Number of kernel launches the last moe_forward enqueued (the pages' decode
+ * loop is dispatch bound, README "Status"). */
 int moe_last_launch_count(const moe_ctx* ctx);
 
 /* Allocation-free routing: router logits, exact top-k with renormalised
@@ -308,6 +333,8 @@ int moe_stack_set_test_flags(moe_stack* s, int flags);
 /* Free the stack's device memory (synchronises the device).  NULL is a no-op. */
 void moe_stack_destroy(moe_stack* s);
 
+/* The last message of `ctx` (NULL: of the calls without a context), and the
+ * name of a status code.  Never NULL. */
 const char* moe_last_error(const moe_ctx* ctx);
 const char* moe_status_string(int status);
 

@@ -217,15 +217,22 @@ __device__ __forceinline__ void tile_task(uint32_t tile, TileGeom geo, int c0, i
   const int r = (lane & 7) + 8 * (mi & 1), dc = mi >> 1;
   const uint32_t rbase = tile + (uint32_t)(r >> 3) * geo.half + (uint32_t)(r & 7) * geo.pitch;
   float o0 = 0.f, o1 = 0.f;
-  auto fold = [&](const float (&acc)[4], int gi) {
+  // row sums (columns in use added) of group gi, folded with its scale and bias
+  auto fold = [&](float a0, float a1, int gi) {
     const uint32_t s0 = sb0[gi], s1 = sb1[gi];
     const float X = xg[gi];
     const float sc0 = bf16_lo(s0), sc1 = bf16_lo(s1);
-    o0 = fmaf(sc0, acc[0] + acc[1], fmaf(bf16_hi(s0) - 128.0f * sc0, X, o0));
-    o1 = fmaf(sc1, acc[2] + acc[3], fmaf(bf16_hi(s1) - 128.0f * sc1, X, o1));
+    o0 = fmaf(sc0, a0, fmaf(bf16_hi(s0) - 128.0f * sc0, X, o0));
+    o1 = fmaf(sc1, a1, fmaf(bf16_hi(s1) - 128.0f * sc1, X, o1));
   };
+  // Four independent accumulator chains per iteration (chunk of the ldmatrix
+  // pair x half of the chunk): an mma.sync result is ready only after a long
+  // latency, so one chain per warp would serialise every MMA of the task.
+#pragma unroll 2
   for (int c = c0; c < c1; c += STEP) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
     for (int cp = 0; cp < STEP; cp += 2) {
       const int cc = c + cp + dc;
@@ -240,17 +247,23 @@ __device__ __forceinline__ void tile_task(uint32_t tile, TileGeom geo, int c0, i
         const uint4 b = *reinterpret_cast<const uint4*>(bcol + (size_t)ch * bstride);
         const uint32_t wg = w[2 * h], wg8 = w[2 * h + 1];
         const uint32_t wg4 = wg >> 4, wg84 = wg8 >> 4;
-        mma16816(acc, code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg4, 0), code_pair(wg84, 0),
-                 b.x, b.y);
-        mma16816(acc, code_pair(wg >> 8, 0), code_pair(wg8 >> 8, 0), code_pair(wg4 >> 8, 0),
-                 code_pair(wg84 >> 8, 0), b.z, b.w);
+        mma16816(acc[2 * h], code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg4, 0),
+                 code_pair(wg84, 0), b.x, b.y);
+        mma16816(acc[2 * h + 1], code_pair(wg >> 8, 0), code_pair(wg8 >> 8, 0),
+                 code_pair(wg4 >> 8, 0), code_pair(wg84 >> 8, 0), b.z, b.w);
         if (CPG == 1) {
-          fold(acc, ch);
-          acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+          const float(&p)[4] = acc[2 * h];
+          const float(&q)[4] = acc[2 * h + 1];
+          fold((p[0] + p[1]) + (q[0] + q[1]), (p[2] + p[3]) + (q[2] + q[3]), ch);
         }
       }
     }
-    if (CPG > 1) fold(acc, c >> LCPG);
+    if (CPG > 1)
+      fold(((acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1])) +
+               ((acc[2][0] + acc[2][1]) + (acc[3][0] + acc[3][1])),
+           ((acc[0][2] + acc[0][3]) + (acc[1][2] + acc[1][3])) +
+               ((acc[2][2] + acc[2][3]) + (acc[3][2] + acc[3][3])),
+           c >> LCPG);
   }
   out0 = o0;
   out1 = o1;
@@ -751,20 +764,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         __syncwarp();
       }
     }
+    // the slots first: the copies wait for them; the weights come later, off
+    // the critical path
     if (warp == 0) {
-      const float w = renormalised_weight(s_sval, k);
       if (lane < k) {
         const int e = s_sidx[lane];
         const int slot = table ? s_tab[e] : e;
         const bool good = slot >= 0 && slot < D.n_slots;
         s_idx[lane] = e;
-        s_w[lane] = w;
         s_slot[lane] = good ? slot : -1;
-        if (c == 0) {
-          if (!good) record_error(a.err, MOE_ERR_SLOT);
-          a.topk_idx[(size_t)l * k + lane] = e;
-          a.topk_w[(size_t)l * k + lane] = w;
-        }
+        if (c == 0 && !good) record_error(a.err, MOE_ERR_SLOT);
       }
       STAMP(23);
     }
@@ -822,6 +831,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
                           D.pool + (uint64_t)s_slot[j] * D.stride + D.d_sb + (size_t)r0 * IG * 4,
                           16u * IG * 4, &mbar[kMbarDown]);
           }
+        }
+      }
+    }
+    // renormalised weights (read by the combine, after the h exchange)
+    if (warp == 0) {
+      const float w = renormalised_weight(s_sval, k);
+      if (lane < k) {
+        s_w[lane] = w;
+        if (c == 0) {
+          a.topk_idx[(size_t)l * k + lane] = s_idx[lane];
+          a.topk_w[(size_t)l * k + lane] = w;
         }
       }
     }
@@ -953,35 +973,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
       STAMP(16);
       __syncthreads();
       STAMP(11);
-      // y rows in a fixed order: routed experts by rank, then the shared one
-      if (tid < 8) {
-        float yv[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 2 * tid + q;
-          float acc = 0.f;
-          for (int j = 0; j <= k; ++j) {
-            if (j < k && s_slot[j] < 0) continue;
-            float v = 0.f;
-            for (int sp = 0; sp < nsplit_d; ++sp) v += s_pdn[(j * nsplit_d + sp) * 16 + m];
-            acc = fmaf(j < k ? s_w[j] : *s_g, v, acc);
-          }
-          yv[q] = acc;
+      // y rows, all threads: thread (m = tid / 16, jl = tid % 16) takes row m's
+      // experts jl, jl + 16, ... (the shared one is j = k), then a fixed
+      // butterfly over the 16 lanes of the row (deterministic)
+      {
+        const int m = tid >> 4, jl = tid & 15;
+        float part = 0.f;
+        for (int j = jl; j <= k; j += 16) {
+          if (j < k && s_slot[j] < 0) continue;
+          float v = 0.f;
+          for (int sp = 0; sp < nsplit_d; ++sp) v += s_pdn[(j * nsplit_d + sp) * 16 + m];
+          part = fmaf(j < k ? s_w[j] : *s_g, v, part);
         }
-        const uint32_t ybits =
-            (uint32_t)f32_to_bf16_rne(yv[0]) | ((uint32_t)f32_to_bf16_rne(yv[1]) << 16);
-        const int wpos = r0 / 2 + tid;
-        if (a.y) reinterpret_cast<uint32_t*>(a.y + (size_t)l * H)[wpos] = ybits;
-        if (a.chain) {
-          const uint32_t xb = s_x[wpos];
-          const float n0 = __fadd_rn(bf16_lo(xb), bf16_lo(ybits));
-          const float n1 = __fadd_rn(bf16_hi(xb), bf16_hi(ybits));
-          const uint32_t nb =
-              (uint32_t)f32_to_bf16_rne(n0) | ((uint32_t)f32_to_bf16_rne(n1) << 16);
-          if (l + 1 < L)
-            __stcg(reinterpret_cast<uint32_t*>(a.ws.xt) + wpos, nb);
-          else if (a.x_out)
-            reinterpret_cast<uint32_t*>(a.x_out)[wpos] = nb;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        const float y1 = __shfl_sync(0xffffffffu, part, 16);  // row 2 warp + 1
+        if (lane == 0) {
+          const uint32_t ybits =
+              (uint32_t)f32_to_bf16_rne(part) | ((uint32_t)f32_to_bf16_rne(y1) << 16);
+          const int wpos = r0 / 2 + warp;
+          if (a.y) reinterpret_cast<uint32_t*>(a.y + (size_t)l * H)[wpos] = ybits;
+          if (a.chain) {
+            const uint32_t xb = s_x[wpos];
+            const float n0 = __fadd_rn(bf16_lo(xb), bf16_lo(ybits));
+            const float n1 = __fadd_rn(bf16_hi(xb), bf16_hi(ybits));
+            const uint32_t nb =
+                (uint32_t)f32_to_bf16_rne(n0) | ((uint32_t)f32_to_bf16_rne(n1) << 16);
+            if (l + 1 < L)
+              __stcg(reinterpret_cast<uint32_t*>(a.ws.xt) + wpos, nb);
+            else if (a.x_out)
+              reinterpret_cast<uint32_t*>(a.x_out)[wpos] = nb;
+          }
         }
         STAMP(17);
       }
