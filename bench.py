@@ -57,6 +57,9 @@ def parse():
                    help="one-token workloads: 'stack' chains the layers (RMSNorm + residual) "
                         "in one persistent launch per token; 'layers' runs independent "
                         "layers, one moe_forward each (auto: stack)")
+    p.add_argument("--phases", action="store_true",
+                   help="one-token stacks: build the instrumented library (per-phase SM cycle "
+                        "stamps) and print each phase's duration instead of the bench line")
     p.add_argument("--profile", action="store_true",
                    help="short run for profilers: no clock-warming loop, no end-to-end or "
                         "stage timing, no CPU baseline")
@@ -710,9 +713,77 @@ def run_ours_stack(args, wl):
         torch.distributed.destroy_process_group()
 
 
+PHASES = [(0, "start"), (1, "input"), (25, "router_dots"), (2, "router"), (8, "logits_in"),
+          (7, "sel_minmax"), (13, "sel_scan"), (14, "sel_cand"), (21, "rank"), (22, "certified"),
+          (23, "slots"), (3, "select"), (24, "gu_first_task"), (9, "gu_tasks"), (4, "gateup"),
+          (12, "h_exchange"), (5, "h_staged"), (10, "dn_data"), (20, "dn_first_task"),
+          (16, "dn_tasks"), (11, "down"), (17, "y_written"), (18, "x_arrive"), (19, "sync"),
+          (6, "end")]
+
+
+def run_phases(args, wl):
+    """Per-phase durations of the persistent decode kernel on a one-token stack:
+    thread 0's SM cycle counter at each phase (an instrumented build of the
+    library), median over CTAs and over the inner layers of the stack."""
+    import torch
+
+    import int4_routed_expert_decode_gb300 as moe
+    from int4_routed_expert_decode_gb300 import build as moe_build
+    here = os.path.join(ROOT, "int4_routed_expert_decode_gb300")
+    moe.LIB_PATH = moe_build.build(defines=("MOE_DECODE_STAMPS",),
+                                   lib_path=os.path.join(here, "_build", "stamps", "libmoe_stamps.so"),
+                                   obj_dir=os.path.join(here, "_build", "stamps"))
+    L = moe.lib()
+    import ctypes
+    L.moe_debug_stack_stamps.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    torch.cuda.set_device(0)
+    NL = args.layers or 16
+    layers = [moe.MoELayer(wl.E, wl.k, wl.H, wl.I, wl.Is, wl.G,
+                           weights=synth.layer_weights(0, wl.wid, l, wl.shape), max_T=1)
+              for l in range(NL)]
+    norms = [torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16)
+             for g in stack_norm_weights(wl, NL)]
+    st = moe.MoEStack(layers, norms, STACK_EPS)
+    xs = [torch.from_numpy(synth.tokens(0, wl.wid, 0, s, 1, wl.H)[0].view(np.int16)).cuda()
+          .view(torch.bfloat16) for s in range(4)]
+    for i in range(max(args.warmup, 3) + args.steps):
+        st.forward(xs[i % 4])
+    torch.cuda.synchronize()
+    assert st.status() == moe.MOE_OK
+    nC = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = np.zeros(NL * nC * 32, np.uint64)
+    L.moe_debug_stack_stamps(st.stack, buf.ctypes.data, NL * nC * 32)
+    a = buf.reshape(NL, nC, 32).astype(np.int64)
+    clk = ClockSampler(0).start()  # the SM clock under the same load converts cycles to us
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < 1.5:
+        st.forward(xs[i % 4])
+        i += 1
+        if i % 32 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    mhz = clk.stop()["sm_mhz"] or 2070.0
+    out = {"workload": wl.name, "layers": NL, "sm_mhz": mhz,
+           "note": "us from the layer's start, per CTA (thread 0), median over CTAs and "
+                   "layers 1..L-2; dn_* only on CTAs with a down tile", "phases": {}}
+    for slot, name in PHASES:
+        v = [(a[l, c, slot] - a[l, c, 0]) / mhz for l in range(1, NL - 1) for c in range(nC)
+             if a[l, c, slot] and a[l, c, 0]]
+        if v:
+            out["phases"][name] = round(float(np.median(v)), 3)
+    per = [np.median((a[l + 1, :, 0] - a[l, :, 0]) / mhz) for l in range(1, NL - 1)]
+    out["layer_period_us"] = round(float(np.median(per)), 3)
+    print(json.dumps(out), flush=True)
+    st.close()
+
+
 def main():
     args = parse()
     wl = synth.WORKLOADS[args.workload]
+    if args.phases:
+        run_phases(args, wl)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
     elif stack_mode(args, wl):

@@ -233,6 +233,18 @@ int64_t moe_device_bytes(const moe_ctx* ctx);
  * loop is dispatch bound, README "Status"). */
 int moe_last_launch_count(const moe_ctx* ctx);
 
+/* The tensor-core router (T >= 128 tokens, E a multiple of 128) filters
+ * candidates with a margin d = 2^-10 |x|_2 max_e |Wr_e|_2 + 2^-22 max|prior|
+ * around approximate logits and certifies the candidates; a token whose
+ * measured approximation error on a candidate exceeds d/8 has every expert
+ * certified instead.  This reads (synchronising the device) and resets what
+ * the calls since the last read saw: the largest |approximate - certified
+ * fp32 logit| over the candidates, divided by |x|_2 max_e |Wr_e|_2, and the
+ * number of tokens that fell back.  Either
+ * pointer may be NULL.  A diagnostic; the pages have no counterpart.
+ * Errors: INVALID_ARG, NOT_RESERVED, CUDA. */
+int moe_router_check_stats(moe_ctx* ctx, float* max_error_ratio, int* fallback_tokens);
+
 /* Allocation-free routing: router logits, exact top-k with renormalised
  * weights, and the shared-expert sigmoid gate for T tokens, with no context
  * and no device allocation of any kind.  The pages have no counterpart: this

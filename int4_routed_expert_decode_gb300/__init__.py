@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
     "moe_route_static", "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
     "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags", "moe_stack_destroy",
+    "moe_router_check_stats",
 )
 
 
@@ -102,6 +103,9 @@ def lib():
     L.moe_stack_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_stack_get_status.argtypes = [vp, vp]
     L.moe_stack_set_test_flags.argtypes = [vp, i32]
+    L.moe_router_check_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_int)]
+    L.moe_router_check_stats.restype = i32
     L.moe_stack_destroy.argtypes = [vp]
     L.moe_stack_destroy.restype = None
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
@@ -268,6 +272,14 @@ def moe_route_static(x, T: int, router_w, router_bias, shared_gate_w, E: int, k:
     _check(lib().moe_route_static(_addr(x), T, _addr(router_w), _addr(router_bias),
                                   _addr(shared_gate_w), E, k, hidden, _addr(topk_idx),
                                   _addr(topk_w), _addr(shared_gate), _stream(stream)))
+
+
+def moe_router_check_stats(ctx: int) -> tuple[float, int]:
+    """(largest measured tensor-core router error / (|x| max|Wr|), fallback tokens)
+    since the last read; resets both (see include/moe.h)."""
+    r, n = ctypes.c_float(), ctypes.c_int()
+    _check(lib().moe_router_check_stats(ctx, ctypes.byref(r), ctypes.byref(n)), ctx)
+    return r.value, n.value
 
 
 def moe_stack_create(layer_ctxs, norm_w=None, eps: float = 1e-6) -> int:

@@ -357,6 +357,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_o = take(rows * d.H * 4);
   const uint64_t o_err = take(4);
   const uint64_t o_bar = take(kSyncWords * 8);
+  const uint64_t o_rstats = take(8);
   const uint64_t o_tiles = take((uint64_t)prefill_max_tiles(d, max_T) * 16);
   const uint64_t o_ntiles = take(4);
   const uint64_t o_dlayer = take(sizeof(DecLayer));
@@ -388,6 +389,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.o = (float*)(base + o_o);
   c.err = (int32_t*)(base + o_err);
   c.ws.bar = (unsigned long long*)(base + o_bar);
+  c.ws.rstats = (uint32_t*)(base + o_rstats);
   c.ws.tiles = base + o_tiles;
   c.ws.n_tiles = (int32_t*)(base + o_ntiles);
   c.dec_layer = (DecLayer*)(base + o_dlayer);
@@ -608,6 +610,23 @@ void moe_destroy(moe_ctx* ctx) {
     free_workspace(ctx->c);
   }
   delete ctx;
+}
+
+int moe_router_check_stats(moe_ctx* ctx, float* max_error_ratio, int* fallback_tokens) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  Ctx& c = ctx->c;
+  if (!c.ws.rstats) return set_msg(ctx, MOE_ERR_NOT_RESERVED, "moe_reserve has not been called");
+  DeviceGuard guard(c.device);
+  uint32_t v[2] = {0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(v, c.ws.rstats, 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(c.ws.rstats, 0, 8);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router check stats");
+  float r;
+  std::memcpy(&r, &v[0], 4);
+  if (max_error_ratio) *max_error_ratio = r;
+  if (fallback_tokens) *fallback_tokens = (int)v[1];
+  return MOE_OK;
 }
 
 // ---------------------------------------------------------------- stacks

@@ -364,8 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   const int dt0 = part(H / 16, c, a.inv_nc), dt1 = part(H / 16, c + 1, a.inv_nc);
   const bool has_down = dt1 > dt0;  // at most one 16-row tile of y per CTA (the plan checks)
   const int r0 = 16 * dt0;
-  // k-splits of whole groups and of an even number of chunks (ldmatrix takes two)
-  const int nsplit_gu = min(4, HC / max(2, 1 << LCPG)), nsplit_d = min(4, IC / max(2, 1 << LCPG));
+  // gate/up tasks: k-splits of whole groups and of an even number of chunks
+  // (ldmatrix takes two); a down task is one expert's whole row block
+  // (measured: fewer, longer down tasks cost less per chunk)
+  const int nsplit_gu = min(4, HC / max(2, 1 << LCPG)), nsplit_d = 1;
   const bool dswz = I / 2 >= 128;
   const int ncbd = dswz ? I / 256 : 1;
   // gate/up tiles: two units of 8 rows, each one TMA box [column block][row][128 B]
@@ -1056,8 +1058,8 @@ bool plan_smem(const Dims& d, int nC, bool chain, DecSmem& s) {
   if (tiles_max > kMaxTiles || rw_max + 1 > kThreads) return false;
   const int S = std::min(8, H / 256);
   const int cpg2 = std::max(2, G / 32);
-  const int nsg = std::min(4, (H / 32) / cpg2), nsd = std::min(4, (I / 32) / cpg2);
-  if (nsd < 1 || nsg < 1) return false;
+  const int nsg = std::min(4, (H / 32) / cpg2), nsd = 1;
+  if (nsg < 1 || (I / 32) % cpg2 != 0) return false;
   s.mbar = take(kNumMbar * 8, 16);
   s.misc = take(1024, 16);
   s.part = take((uint64_t)(rw_max + 1) * S * 4, 16);

@@ -96,6 +96,8 @@ struct Workspace {
   float* h;           // [max_T*k + max_T][maxI] fp32 SwiGLU activations
   float* o;           // [max_T*k + max_T][H]    fp32 expert outputs
   unsigned long long* bar;  // fused kernel: grid-barrier arrival counter (monotonic)
+  uint32_t* rstats;   // tensor-core router check: [0] max observed error / (|x| max|Wr|)
+                      // (float bits), [1] tokens that fell back to certifying every expert
   void* tiles;        // [max tiles] prefill work tiles (16 bytes each)
   int32_t* n_tiles;   // [1]
 };

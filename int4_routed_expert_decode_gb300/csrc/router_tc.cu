@@ -9,12 +9,21 @@
 //    selection of routing_common.cuh orders them (ties to the lower id); the
 //    weights are the renormalised softmax of the selected logits.
 //
-// Why the filter is safe: the tensor core multiplies bf16 operands exactly and
-// accumulates in fp32, so |a - l| is far below d = 2^-10 |x||w| >= 2^-10 sum |x w|
-// (it would take an accumulator with fewer than 10 correct bits of the sum of
-// magnitudes -- less than bf16 arithmetic has -- to reach d).  An expert whose approximate logit is below the
-// k-th largest minus 2d is then below k experts in exact value, so it cannot
-// be selected; every expert that can is recomputed and certified.
+// Why the filter is safe.  If |a_e - l_e| <= delta for every expert, the k-th
+// largest approximate logit is within delta of the k-th largest exact one, so
+// an expert that can be selected has a_e >= (k-th approximate) - 2 delta:
+// the filter keeps it whenever delta <= d.  Error model of the tensor cores
+// (kind::f16, fp32 accumulation): bf16 x bf16 products are exact; each k-step
+// of 16 products is summed after aligning to the largest with at least 23
+// kept bits (truncation), then added to the fp32 accumulator with rounding.
+// That gives delta <= (16 2^-23 + (H/16) 2^-24) sum|x w| <= (2^-19 + H 2^-28)
+// |x| |w| (Cauchy-Schwarz) -- at H = 8192 about 2^-15 |x||w|, 32 times below
+// the accumulation term of d = 2^-10 |x| max_e|Wr_e| + 2^-22 max|prior| (the
+// second term covers the rounding of the prior's addition).  The model is not
+// taken on trust: every candidate's certified logit measures the error on
+// that expert (at least |a - l| - bound), and a token whose measured error
+// exceeds d/8 falls back to certifying all E experts.  The largest observed
+// |a - l| and the number of fallbacks are kept for moe_router_check_stats.
 #include <cuda.h>
 
 #include "device_util.cuh"
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
     const float* __restrict__ wnorm, const float* __restrict__ gate_z,
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ router_w,
     const float* __restrict__ prior, int T, int E, int H, int k, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, float* __restrict__ gate) {
+    float* __restrict__ topk_w, float* __restrict__ gate, uint32_t* __restrict__ rstats) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCandWarps + warp;
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
   // the k-th largest approximate logit (entries in lane-major order)
   uint32_t key[MAXV];
   int id[MAXV];
-  float wmax = 0.f;
+  float wmax = 0.f, pmax = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int e = lane * MAXV + i;
@@ -222,9 +231,13 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
     if (v != v) v = -INFINITY;
     key[i] = e < E ? f32_key(v) : 0u;
     id[i] = e < E ? e : 0x7FFFFFFF;
-    if (e < E) wmax = fmaxf(wmax, __ldg(wnorm + e));
+    if (e < E) {
+      wmax = fmaxf(wmax, __ldg(wnorm + e));
+      if (prior) pmax = fmaxf(pmax, fabsf(__ldg(prior + e)));
+    }
   }
   wmax = warp_max(wmax);
+  pmax = warp_max(pmax);
   uint32_t kk[MAXV];
   int ki[MAXV];
 #pragma unroll
@@ -248,7 +261,10 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
       ki[MAXV - 1] = 0x7FFFFFFF;
     }
   }
-  const float d = 0.0009765625f * __ldg(xnorm + t) * wmax;
+  // d bounds |a - l| for every expert: 2^-10 |x| max|Wr| the accumulation
+  // (file comment), 2^-22 max|prior| the rounding of the prior's addition
+  const float xn = __ldg(xnorm + t);
+  const float d = 0.0009765625f * xn * wmax + 2.384185791015625e-07f * pmax;
   const float cut = key_f32(kth) - 2.0f * d;
   // candidates, in expert order
   int n = 0;
@@ -263,16 +279,43 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
   }
   __syncwarp();
   // certified logits of the candidates, four at a time (8 lanes each)
-  for (int i = 0; i < n; i += 4) {
-    const int g = lane >> 3, e = i + g < n ? cid[i + g] : -1;
-    float l, b;
-    tight_logit_group8(x + (size_t)t * H, router_w, H, prior, e, l, b);
-    if ((lane & 7) == 0 && e >= 0) {
-      cl[i + g] = l;
-      cb[i + g] = b;
+  auto certify = [&]() {
+    for (int i = 0; i < n; i += 4) {
+      const int g = lane >> 3, e = i + g < n ? cid[i + g] : -1;
+      float l, b;
+      tight_logit_group8(x + (size_t)t * H, router_w, H, prior, e, l, b);
+      if ((lane & 7) == 0 && e >= 0) {
+        cl[i + g] = l;
+        cb[i + g] = b;
+      }
     }
+    __syncwarp();
+  };
+  certify();
+  // Run-time check of the error model on the candidates: the tensor cores'
+  // error on expert e is at least |a_e - l_e| - b_e.  If one exceeds d/8 the
+  // model does not hold for this token, and every expert is certified.
+  // (the statistic kept is the plain difference |a - l|, error of l included)
+  float worst = 0.f, diff = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    const float dd = fabsf(__ldcg(arow + cid[i]) - cl[i]);
+    diff = fmaxf(diff, dd);
+    worst = fmaxf(worst, dd - cb[i]);
   }
-  __syncwarp();
+  worst = warp_max(worst);
+  diff = warp_max(diff);
+  const bool fallback = worst > 0.125f * d;
+  if (lane == 0 && rstats) {
+    const float denom = xn * wmax;
+    if (denom > 0.f) atomicMax(rstats, __float_as_uint(diff / denom));
+    if (fallback) atomicAdd(rstats + 1, 1u);
+  }
+  if (fallback) {
+    n = E;
+    for (int e = lane; e < E; e += 32) cid[e] = e;
+    __syncwarp();
+    certify();
+  }
   int* sel_idx;
   float* sel_val;
   // one candidate per lane when they fit (the usual case), else MAXV per lane
@@ -373,7 +416,7 @@ cudaError_t launch_router_candidates(const Ctx& c, const FwdArgs& a, cudaStream_
 #define MOE_CAND(MV)                                                                            \
   router_candidates_kernel<MV><<<grid, kCandWarps * 32, smem, st>>>(                           \
       c.ws.logits, c.ws.xnorm, c.ws.wnorm, c.ws.gate_z, a.x, c.router_w, c.router_bias, a.T,    \
-      d.E, d.H, d.k, a.topk_idx, a.topk_w, c.ws.gate)
+      d.E, d.H, d.k, a.topk_idx, a.topk_w, c.ws.gate, c.ws.rstats)
   if (d.E <= 128) MOE_CAND(4);
   else if (d.E <= 256) MOE_CAND(8);
   else if (d.E <= 512) MOE_CAND(16);
