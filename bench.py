@@ -57,6 +57,9 @@ def parse():
                    help="one-token workloads: 'stack' chains the layers (RMSNorm + residual) "
                         "in one persistent launch per token; 'layers' runs independent "
                         "layers, one moe_forward each (auto: stack)")
+    p.add_argument("--pool-slots", type=int, default=0,
+                   help="bounded slot pool of this many resident experts per layer (the rest "
+                        "in pinned host memory, LFU + recency eviction); implies --mode layers")
     p.add_argument("--phases", action="store_true",
                    help="one-token stacks: build the instrumented library (per-phase SM cycle "
                         "stamps) and print each phase's duration instead of the bench line")
@@ -291,7 +294,7 @@ def run_reference(args, wl):
 
 
 def stack_mode(args, wl):
-    return wl.T == 1 and args.mode in ("auto", "stack")
+    return wl.T == 1 and args.mode in ("auto", "stack") and not args.pool_slots
 
 
 STACK_EPS = 1e-6
@@ -368,6 +371,8 @@ def run_ours(args, wl):
         layer = moe.MoELayer(wl.E, wl.k, H, wl.I, wl.Is, wl.G, weights=W, max_T=T)
         if args.path:
             moe.moe_set_path(layer.ctx, args.path)
+        if args.pool_slots:
+            moe.moe_pool_enable(layer.ctx, args.pool_slots)
         layers.append(layer)
         del W
     x_all = torch.empty((S, L, T, H), dtype=torch.bfloat16, device="cuda")
@@ -432,6 +437,7 @@ def run_ours(args, wl):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        pool0 = [moe.moe_pool_stats(l.ctx) for l in layers] if args.pool_slots else None
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         for i in range(args.steps):
@@ -442,6 +448,17 @@ def run_ours(args, wl):
         if world > 1:
             torch.distributed.barrier()
         ms = ev0.elapsed_time(ev1)
+        pool = None
+        if args.pool_slots:
+            pool1 = [moe.moe_pool_stats(l.ctx) for l in layers]
+            hits = sum(b["hits"] - a["hits"] for a, b in zip(pool0, pool1))
+            misses = sum(b["misses"] - a["misses"] for a, b in zip(pool0, pool1))
+            pool = {"slots_per_layer": args.pool_slots, "experts_per_layer": wl.E,
+                    "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+                    "fills_from_pinned_host_per_step": misses / args.steps,
+                    "overflows": sum(b["overflows"] - a["overflows"]
+                                     for a, b in zip(pool0, pool1)),
+                    "distinct_step_inputs": S}
     clk = clocks.stop()
     # per-stage device times of layer 0 (eager, same stream, after the timed region)
     stages = {} if args.profile else stage_times(
@@ -535,6 +552,8 @@ def run_ours(args, wl):
         "clocks": clk, "gpu_launches": args.steps * L * launches_per_layer,
         "parity_spot_check": parity,
     }
+    if pool is not None:
+        line["pool"] = pool
     if rank == 0:
         print(json.dumps(line), flush=True)
     for layer in layers:

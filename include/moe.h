@@ -233,6 +233,39 @@ int64_t moe_device_bytes(const moe_ctx* ctx);
  * loop is dispatch bound, README "Status"). */
 int moe_last_launch_count(const moe_ctx* ctx);
 
+/* ---------------------------------------------------------------- slot pool
+ * The pages keep the routed experts in storage and cache the hot ones "in a
+ * bounded pool with LFU plus recency eviction" (README "How it works";
+ * creativeainews, "How Expert Streaming Works").  moe_pool_enable moves the
+ * loaded experts (n_slots >= E, slot e = expert e) into pinned, device-mapped
+ * host memory -- the store, read by the GPU over NVLink-C2C -- and keeps
+ * `slots` of them (1 <= slots < E, at most 65534) in the device pool, empty
+ * at first.  From then on every moe_forward (expert_slot_table must be NULL)
+ * routes, then updates the pool on the stream with no host synchronisation:
+ *   - a selected expert in the pool is a hit: its frequency grows by the
+ *     number of (token, expert) pairs routed to it, its last use is this call;
+ *   - the misses, in ascending expert id, take an empty slot (lowest first),
+ *     else evict among the slots this call does not need the one with the
+ *     lowest frequency, then the least recent use, then the lowest slot;
+ *     the evicted expert leaves the table, the new one is copied in;
+ *   - a call that needs more distinct experts than there are slots leaves the
+ *     excess unmapped (counted as overflows; the device records MOE_ERR_SLOT
+ *     and those experts are skipped).
+ * y is the same as with every expert resident.  Calls with a pool use the
+ * multi-launch path (router, top-k, pool, permutation, experts), also for
+ * T = 1; stacks do not take pooled layers.  Synchronous.
+ * Errors: INVALID_ARG (sizes, already enabled, n_slots < E), NOT_LOADED,
+ * OOM/CUDA (allocations). */
+int moe_pool_enable(moe_ctx* ctx, int slots);
+
+/* Counters since moe_pool_enable, synchronising the device: out[0] calls,
+ * out[1] hits, out[2] misses (fills), out[3] evictions, out[4] overflows.
+ * The hit rate is hits / (hits + misses). */
+int moe_pool_stats(moe_ctx* ctx, int64_t* out);
+
+/* The pool's current table (int32 [E], host): slot of expert e or -1. */
+int moe_pool_table(moe_ctx* ctx, int32_t* table_out);
+
 /* The tensor-core router (T >= 128 tokens, E a multiple of 128) filters
  * candidates with a margin d = 2^-10 |x|_2 max_e |Wr_e|_2 + 2^-22 max|prior|
  * around approximate logits and certifies the candidates; a token whose

@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_last_launch_count", "moe_last_error", "moe_status_string", "moe_destroy",
     "moe_route_static", "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
     "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags", "moe_stack_destroy",
-    "moe_router_check_stats",
+    "moe_router_check_stats", "moe_pool_enable", "moe_pool_stats", "moe_pool_table",
 )
 
 
@@ -106,6 +106,12 @@ def lib():
     L.moe_router_check_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_int)]
     L.moe_router_check_stats.restype = i32
+    L.moe_pool_enable.argtypes = [vp, i32]
+    L.moe_pool_enable.restype = i32
+    L.moe_pool_stats.argtypes = [vp, vp]
+    L.moe_pool_stats.restype = i32
+    L.moe_pool_table.argtypes = [vp, vp]
+    L.moe_pool_table.restype = i32
     L.moe_stack_destroy.argtypes = [vp]
     L.moe_stack_destroy.restype = None
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
@@ -272,6 +278,23 @@ def moe_route_static(x, T: int, router_w, router_bias, shared_gate_w, E: int, k:
     _check(lib().moe_route_static(_addr(x), T, _addr(router_w), _addr(router_bias),
                                   _addr(shared_gate_w), E, k, hidden, _addr(topk_idx),
                                   _addr(topk_w), _addr(shared_gate), _stream(stream)))
+
+
+def moe_pool_enable(ctx: int, slots: int):
+    _check(lib().moe_pool_enable(ctx, slots), ctx)
+
+
+def moe_pool_stats(ctx: int) -> dict:
+    out = np.zeros(5, np.int64)
+    _check(lib().moe_pool_stats(ctx, out.ctypes.data), ctx)
+    return {"calls": int(out[0]), "hits": int(out[1]), "misses": int(out[2]),
+            "evictions": int(out[3]), "overflows": int(out[4])}
+
+
+def moe_pool_table(ctx: int, E: int) -> np.ndarray:
+    out = np.zeros(E, np.int32)
+    _check(lib().moe_pool_table(ctx, out.ctypes.data), ctx)
+    return out
 
 
 def moe_router_check_stats(ctx: int) -> tuple[float, int]:

@@ -66,7 +66,14 @@ void free_dev(T*& p) {
   p = nullptr;
 }
 
+void free_pool(Ctx& c) {
+  if (c.pl.store) cudaFreeHost(c.pl.store);
+  if (c.pl.dev) cudaFree(c.pl.dev);
+  c.pl = PoolState{};
+}
+
 void free_weights(Ctx& c) {
+  free_pool(c);
   free_dev(c.router_w);
   free_dev(c.router_bias);
   free_dev(c.shared_gate_w);
@@ -427,9 +434,12 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   if (T > c.max_T) return set_msg(ctx, MOE_ERR_NOT_RESERVED, "T=%d > reserved max_T=%d", T, c.max_T);
   if (!x || !y || !topk_idx || !topk_w)
     return set_msg(ctx, MOE_ERR_INVALID_ARG, "x, y, topk_idx and topk_w must be non-NULL");
-  if (!expert_slot_table && c.n_slots < c.d.E)
+  if (c.pl.slots && expert_slot_table)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "the slot pool keeps its own table: pass NULL");
+  if (!c.pl.slots && !expert_slot_table && c.n_slots < c.d.E)
     return set_msg(ctx, MOE_ERR_INVALID_ARG,
                    "identity slot table needs n_slots (%d) >= E (%d)", c.n_slots, c.d.E);
+  if (c.pl.slots) expert_slot_table = c.pl.table;
   if (((uintptr_t)x & 15) != 0)
     return set_msg(ctx, MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   const size_t xb = (size_t)T * c.d.H * 2;
@@ -440,7 +450,9 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   cudaStream_t st = (cudaStream_t)stream;
   FwdArgs a{(const uint16_t*)x, T, expert_slot_table, (uint16_t*)y, topk_idx, topk_w, perm, offsets};
   int launches = 0;
-  const bool fused_ok = T == 1 && (c.dec_ok || fused_decode_supported(c));
+  // the slot pool updates the table between routing and the experts: not in
+  // the single-launch decode kernels
+  const bool fused_ok = T == 1 && !c.pl.slots && (c.dec_ok || fused_decode_supported(c));
   const bool prefill_ok = prefill_supported(c.d);
   if (c.path == MOE_PATH_DECODE && !fused_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
@@ -481,6 +493,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
     e = launch_router(c, a, st, &launches);
     record_mark(c, MOE_MARK_LOGITS, st);
     if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+    if (e == cudaSuccess && c.pl.slots) e = launch_pool_update(c, a.topk_idx, T * c.d.k, st, &launches);
     record_mark(c, MOE_MARK_ROUTED, st);
     if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
     if (e == cudaSuccess && use_prefill) e = launch_prefill_plan(c, a, st, &launches);
@@ -612,6 +625,98 @@ void moe_destroy(moe_ctx* ctx) {
   delete ctx;
 }
 
+int moe_pool_enable(moe_ctx* ctx, int slots) {
+  if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
+  Ctx& c = ctx->c;
+  const int E = c.d.E;
+  if (!c.pool) return set_msg(ctx, MOE_ERR_NOT_LOADED, "moe_load_weights has not been called");
+  if (c.pl.slots) return set_msg(ctx, MOE_ERR_INVALID_ARG, "the slot pool is already enabled");
+  if (c.n_slots < E)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG,
+                   "the pool takes its store from the loaded experts: n_slots (%d) must be >= E (%d)",
+                   c.n_slots, E);
+  if (slots < 1 || slots >= E || slots > 65534)
+    return set_msg(ctx, MOE_ERR_INVALID_ARG, "slots=%d not in [1, min(E - 1, 65534)]", slots);
+  DeviceGuard guard(c.device);
+  cudaDeviceSynchronize();
+  const size_t blob = c.ex.stride, store_bytes = (size_t)E * blob;
+  PoolState p{};
+  p.slots = slots;
+  cudaError_t e = cudaHostAlloc(&p.store, store_bytes, cudaHostAllocMapped);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "pinned expert store");
+  void* dptr = nullptr;
+  e = cudaHostGetDevicePointer(&dptr, p.store, 0);
+  if (e == cudaSuccess) e = cudaMemcpy(p.store, c.pool, store_bytes, cudaMemcpyDeviceToHost);
+  const size_t arr = align256((uint64_t)E * 4) * 3 + align256((uint64_t)slots * 4) * 3 + 256;
+  if (e == cudaSuccess) e = cudaMalloc(&p.dev, arr);
+  uint8_t* newpool = nullptr;
+  if (e == cudaSuccess) e = cudaMalloc(&newpool, (size_t)slots * blob);
+  if (e != cudaSuccess) {
+    if (newpool) cudaFree(newpool);
+    c.pl = p;
+    free_pool(c);
+    return cuda_fail(ctx, e, "slot pool");
+  }
+  p.store_dev = (const uint8_t*)dptr;
+  uint8_t* b = (uint8_t*)p.dev;
+  size_t o = 0;
+  auto take = [&](size_t n) {
+    uint8_t* r = b + o;
+    o += align256(n);
+    return r;
+  };
+  p.table = (int32_t*)take((size_t)E * 4);
+  p.fill_expert = (int32_t*)take((size_t)E * 4);
+  p.fill_slot = (int32_t*)take((size_t)E * 4);
+  p.owner = (int32_t*)take((size_t)slots * 4);
+  p.freq = (uint32_t*)take((size_t)slots * 4);
+  p.last = (uint32_t*)take((size_t)slots * 4);
+  p.state = (uint32_t*)take(8 * 4);
+  e = cudaMemset(p.dev, 0, arr);
+  if (e == cudaSuccess) e = cudaMemset(p.table, 0xFF, (size_t)E * 4);  // every expert unmapped
+  if (e == cudaSuccess) e = cudaMemset(p.owner, 0xFF, (size_t)slots * 4);  // every slot empty
+  if (e != cudaSuccess) {
+    cudaFree(newpool);
+    c.pl = p;
+    free_pool(c);
+    return cuda_fail(ctx, e, "slot pool init");
+  }
+  cudaFree(c.pool);
+  c.pool = newpool;
+  c.n_slots = slots;
+  c.pl = p;
+  c.weight_bytes -= (int64_t)(E - slots) * (int64_t)blob;
+  // the persistent decode kernel is not used with a pool (it reads no table
+  // updated between its phases); its descriptor would name the old pool
+  c.dec_ok = 0;
+  return MOE_OK;
+}
+
+int moe_pool_stats(moe_ctx* ctx, int64_t* out) {
+  if (!ctx || !out) return set_msg(ctx, MOE_ERR_INVALID_ARG, "ctx or out is NULL");
+  Ctx& c = ctx->c;
+  if (!c.pl.slots) return set_msg(ctx, MOE_ERR_INVALID_ARG, "no slot pool (moe_pool_enable)");
+  DeviceGuard guard(c.device);
+  uint32_t v[8];
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(v, c.pl.state, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "slot pool stats");
+  for (int i = 0; i < 5; ++i) out[i] = (int64_t)v[i];
+  return MOE_OK;
+}
+
+int moe_pool_table(moe_ctx* ctx, int32_t* table_out) {
+  if (!ctx || !table_out) return set_msg(ctx, MOE_ERR_INVALID_ARG, "ctx or table_out is NULL");
+  Ctx& c = ctx->c;
+  if (!c.pl.slots) return set_msg(ctx, MOE_ERR_INVALID_ARG, "no slot pool (moe_pool_enable)");
+  DeviceGuard guard(c.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(table_out, c.pl.table, (size_t)c.d.E * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "slot pool table");
+  return MOE_OK;
+}
+
 int moe_router_check_stats(moe_ctx* ctx, float* max_error_ratio, int* fallback_tokens) {
   if (!ctx) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "ctx is NULL");
   Ctx& c = ctx->c;
@@ -646,6 +751,8 @@ int moe_stack_create(moe_ctx* const* layers, int L, const uint16_t* const* norm_
     if (!layers[l]) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "layers[%d] is NULL", l);
     const Ctx& c = layers[l]->c;
     if (!c.pool) return set_msg(nullptr, MOE_ERR_NOT_LOADED, "layers[%d] has no weights", l);
+    if (c.pl.slots)
+      return set_msg(nullptr, MOE_ERR_INVALID_ARG, "layers[%d] has a slot pool (not in stacks)", l);
     const Dims& a = layers[0]->c.d;
     if (c.d.E != a.E || c.d.k != a.k || c.d.H != a.H || c.d.I != a.I || c.d.Is != a.Is ||
         c.d.G != a.G || c.device != layers[0]->c.device)

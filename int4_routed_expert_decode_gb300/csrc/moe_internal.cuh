@@ -102,6 +102,22 @@ struct Workspace {
   int32_t* n_tiles;   // [1]
 };
 
+// Bounded slot pool (pool.cu): every expert blob in pinned, device-mapped
+// host memory, `slots` of them resident in the device pool.
+struct PoolState {
+  int slots = 0;                  // 0: no pool (the caller's table or the identity)
+  uint8_t* store = nullptr;       // host: E blobs (cudaHostAlloc, mapped)
+  const uint8_t* store_dev = nullptr;  // its device address
+  void* dev = nullptr;            // one device allocation for the arrays below
+  int32_t* table = nullptr;       // [E] expert -> slot or -1
+  int32_t* owner = nullptr;       // [slots] slot -> expert or -1
+  uint32_t* freq = nullptr;       // [slots]
+  uint32_t* last = nullptr;       // [slots]
+  uint32_t* state = nullptr;      // [8] step, hits, misses, evictions, overflows, last fills
+  int32_t* fill_expert = nullptr; // [E]
+  int32_t* fill_slot = nullptr;   // [E]
+};
+
 struct Ctx {
   int device = -1;
   Dims d{};
@@ -133,6 +149,7 @@ struct Ctx {
   // 2.5 us per layer), so single-layer launches go without it (stacks use it).
   bool cooperative = false;
   unsigned long long* dec_stamps = nullptr;  // phase timestamps (instrumented builds only)
+  PoolState pl{};                     // bounded slot pool (moe_pool_enable)
   int test_flags = 0;                 // MOE_TEST_* hooks
   cudaEvent_t marks[MOE_MARK_COUNT] = {};  // borrowed stage events (moe_set_stage_events)
   int n_marks = 0;
@@ -150,6 +167,9 @@ cudaError_t launch_unpack_expert(const uint8_t* blob, int H, int I, int G, const
                                  uint32_t* gq, uint16_t* gs, uint16_t* gb, uint32_t* uq,
                                  uint16_t* us, uint16_t* ub, uint32_t* dq, uint16_t* ds,
                                  uint16_t* db, cudaStream_t st);
+
+cudaError_t launch_pool_update(const Ctx& c, const int32_t* topk_idx, int P, cudaStream_t st,
+                               int* launches);
 
 struct FwdArgs {
   const uint16_t* x;

@@ -91,3 +91,10 @@ def test_stack_calls_reject_null_arguments(L):
     assert L.moe_stack_get_status(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_stack_set_test_flags(None, 0) == moe.MOE_ERR_INVALID_ARG
     L.moe_stack_destroy(None)
+
+
+def test_pool_calls_reject_null_arguments(L):
+    assert L.moe_pool_enable(None, 4) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pool_stats(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pool_table(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_router_check_stats(None, None, None) == moe.MOE_ERR_INVALID_ARG
