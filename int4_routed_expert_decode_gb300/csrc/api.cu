@@ -414,7 +414,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   if ((e = prepare_router(c)) != cudaSuccess || (e = prepare_general_experts(c)) != cudaSuccess ||
       (e = prepare_fused_decode(c)) != cudaSuccess ||
       (e = decode_prepare(d, c.num_sms, false, &c.dec_ok)) != cudaSuccess ||
-      (e = refresh_decode_layer(c)) != cudaSuccess ||
+      (e = refresh_decode_layer(c)) != cudaSuccess || (e = prepare_batch_decode(c)) != cudaSuccess ||
       (prefill_supported(d) && (e = prepare_prefill(c)) != cudaSuccess)) {
     free_workspace(c);
     return cuda_fail(ctx, e, "kernel attributes");
@@ -453,17 +453,22 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
   // the slot pool updates the table between routing and the experts: not in
   // the single-launch decode kernels
   const bool fused_ok = T == 1 && !c.pl.slots && (c.dec_ok || fused_decode_supported(c));
+  // 2..64 tokens: the batched decode kernels (weights streamed once per used
+  // expert, its tokens in the MMA's columns)
+  const bool bdec_ok = T >= 2 && batch_decode_supported(c, T);
   const bool prefill_ok = prefill_supported(c.d);
-  if (c.path == MOE_PATH_DECODE && !fused_ok)
+  if (c.path == MOE_PATH_DECODE && !fused_ok && !bdec_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
-                   "the fused decode path needs T = 1 and supported sizes");
+                   "the decode path needs T <= 64, no slot pool and supported sizes");
   if (c.path == MOE_PATH_PREFILL && !prefill_ok)
     return set_msg(ctx, MOE_ERR_UNSUPPORTED,
                    "the prefill path needs hidden and 2*inter multiples of 128");
   // measured on GB300: from two tokens on, the grouped GEMMs beat the general
   // CUDA-core kernels (at T = 64 by 30x), so AUTO uses them whenever the sizes allow
-  const bool use_prefill =
-      c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && prefill_ok && T > 1);
+  // (AUTO keeps the grouped GEMMs for T >= 2 until the batched kernels beat them)
+  const bool use_bdec = bdec_ok && c.path == MOE_PATH_DECODE;
+  const bool use_prefill = !use_bdec && (c.path == MOE_PATH_PREFILL ||
+                                         (c.path == MOE_PATH_AUTO && prefill_ok && T > 1));
   cudaError_t e;
   record_mark(c, MOE_MARK_START, st);
   if (fused_ok && c.dec_ok && c.path == MOE_PATH_DECODE) {
@@ -490,17 +495,22 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
                           c.path == kPathFusedV1)) {
     e = launch_fused_decode(c, a, st, &launches);
   } else {
-    e = launch_router(c, a, st, &launches);
-    record_mark(c, MOE_MARK_LOGITS, st);
-    if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+    if (use_bdec) {  // logits, exact top-k and the shared gate in two launches
+      e = launch_batch_route(c, a, st, &launches);
+    } else {
+      e = launch_router(c, a, st, &launches);
+      record_mark(c, MOE_MARK_LOGITS, st);
+      if (e == cudaSuccess) e = launch_topk(c, a, st, &launches);
+    }
     if (e == cudaSuccess && c.pl.slots) e = launch_pool_update(c, a.topk_idx, T * c.d.k, st, &launches);
     record_mark(c, MOE_MARK_ROUTED, st);
     if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
     if (e == cudaSuccess && use_prefill) e = launch_prefill_plan(c, a, st, &launches);
     record_mark(c, MOE_MARK_PERMUTED, st);
     if (e == cudaSuccess)
-      e = use_prefill ? launch_prefill_experts(c, a, st, &launches)
-                      : launch_general_experts(c, a, st, &launches);
+      e = use_bdec      ? launch_batch_decode(c, a, st, &launches)
+          : use_prefill ? launch_prefill_experts(c, a, st, &launches)
+                        : launch_general_experts(c, a, st, &launches);
   }
   record_mark(c, MOE_MARK_END, st);
   c.last_launches = launches;

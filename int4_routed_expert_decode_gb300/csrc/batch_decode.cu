@@ -1,0 +1,765 @@
+// batch_decode.cu -- the experts of the MoE block for 2..64 tokens (batched
+// decode).  After the router, top-k and permutation launches, each used
+// expert's int4 weights stream from HBM once and serve all of its tokens,
+// which ride in the N columns of mma.sync (8 tokens per tile):
+//   bdec_prep_kernel    x in the MMA's k order (bf16) and its group sums
+//   bdec_gateup_kernel  persistent; a unit is 16 interleaved gate/up rows (8
+//                       pairs) of one used expert, or of the shared expert, for
+//                       all of its tokens; SwiGLU; h as bf16 in the same k order
+//                       plus the sum of each 8 values
+//   bdec_hsum_kernel    the group sums of h (fixed order)
+//   bdec_down_kernel    one CTA per 16 rows of y: those rows of every used
+//                       expert's down projection against its tokens' h, then per
+//                       token the routing-weighted combine plus the gated shared
+//                       expert, in a fixed order (deterministic)
+// The weights and the routing are the pages' block (Swiftlet README on the
+// wpnews page, "How it works"; MLX affine int4 groups per its list of what was
+// built); the h rounding to bf16 is the grouped GEMMs' (one bf16 operand).
+#include "device_util.cuh"
+#include "gemv_mma.cuh"
+#include "moe_internal.cuh"
+#include "routing_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace mmag;
+
+constexpr int kBThreads = 256;
+constexpr int kBWarps = 8;
+constexpr int kGuRing = 4;    // gate/up unit slots
+constexpr int kDnBatch = 8;   // down: experts per batch, two batches in flight
+constexpr int kBMaxT = 64;
+// dynamic shared memory limit of these kernels (the down kernel also has a
+// little static shared memory; the sum must stay within the device's 227 KB)
+constexpr int kBSmemMax = 224 * 1024;
+
+struct BArgs {
+  const DecLayer* L;  // maps and pointers of the layer (device)
+  int T, k, E, I, G, P;
+  const int32_t* used;     // [E] used experts, ascending
+  const int32_t* n_used;   // [1]
+  const int32_t* offsets;  // [E+1]
+  const int32_t* perm;     // [P] pair ids sorted by expert
+  const int32_t* inv;      // [P] position of pair p in perm
+  const int32_t* table;    // [E] slots, or null (identity)
+  const uint16_t* x;       // [T][H]
+  uint16_t* xperm;         // [T][H] bf16, k-permuted
+  float* xg;               // [T][H/G]
+  uint16_t* hperm;         // [P + T][I] bf16, k-permuted (rows: perm positions, then shared)
+  float* hs8;              // [P + T][I/8]
+  float* hg;               // [P + T][I/G]
+  const float* topk_w;     // [T][k]
+  const float* gate;       // [T] shared-expert gate
+  uint16_t* y;             // [T][H]
+  int32_t* err;
+  uint32_t gu_slot, gu_sb, part;       // gate/up shared-memory plan (byte offsets)
+  uint32_t dn_slot, dn_sb, ocache;     // down shared-memory plan
+  uint32_t smem_gu, smem_dn;
+};
+
+__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, int32_t* err) {
+  for (int i = 0; i < 10000; ++i)
+    if (ptx::mbar_try_wait_sleep(bar, parity, 100000u)) return;
+  record_error(err, MOE_ERR_TIMEOUT);
+}
+
+// A routed expert's slot, or -1 when its slot is missing or out of range.
+__device__ __forceinline__ int slot_of(const BArgs& a, int e, int n_slots) {
+  const int s = a.table ? a.table[e] : e;
+  return (s >= 0 && s < n_slots) ? s : -1;
+}
+
+// x in the MMA's k order: entry (chunk, t) of 8 bf16 holds inputs
+// 32 chunk + 8 t + (0, 4), (1, 5), (2, 6), (3, 7); and the group sums.
+__global__ void __launch_bounds__(256) bdec_prep_kernel(const uint16_t* __restrict__ x, int H,
+                                                       int G, uint16_t* __restrict__ xperm,
+                                                       float* __restrict__ xg) {
+  const int t = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(xperm + (size_t)t * H);
+  for (int e0 = 0; e0 < H / 8; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    float s8 = 0.f;
+    if (e < H / 8) {
+      const uint4 v = src[e];
+      uint4 o;
+      o.x = __byte_perm(v.x, v.z, 0x5410);
+      o.y = __byte_perm(v.x, v.z, 0x7632);
+      o.z = __byte_perm(v.y, v.w, 0x5410);
+      o.w = __byte_perm(v.y, v.w, 0x7632);
+      dst[e] = o;
+      const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s8 += bf16_lo(ww[q]) + bf16_hi(ww[q]);
+    }
+    // a group's G/8 entries sit on consecutive lanes
+    for (int o = 1; o < (G >> 3); o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
+    if (e < H / 8 && (e & ((G >> 3) - 1)) == 0) xg[(size_t)t * (H / G) + e / (G >> 3)] = s8;
+  }
+}
+
+// hg[row][g] = the sum of h over group g of the row, from the sums of 8.
+__global__ void __launch_bounds__(256) bdec_hsum_kernel(const float* __restrict__ hs8, int rows,
+                                                       int I, int G, float* __restrict__ hg) {
+  const int IG = I / G, per = G / 8;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows * IG) return;
+  const int row = i / IG, g = i - row * IG;
+  float s = 0.f;
+  for (int u = 0; u < per; ++u) s += hs8[(size_t)row * (I / 8) + g * per + u];
+  hg[i] = s;
+}
+
+// One task: chunks [c0, c1) of K of a 16-row tile against 8 token columns.
+// Lane (g = lane / 4, t = lane % 4) loads column g's input (b_src, or zeros
+// when null) and ends with rows g, g + 8 x columns 2t, 2t + 1 in o[0..3]
+// (row g col 2t, row g col 2t+1, row g+8 col 2t, row g+8 col 2t+1).
+//   b_src    this lane's column: 16-byte entries (chunk, t) 64 bytes apart
+//   sb0/1    (scale | bias << 16) words of rows g and g + 8, one per group
+//   xa, xb   group sums of columns 2t and 2t + 1 (null: column unused)
+template <int LCPG>
+__device__ __forceinline__ void tile_task_n(uint32_t tile, TileGeom geo, int c0, int c1,
+                                            const uint4* b_src, const uint32_t* sb0,
+                                            const uint32_t* sb1, const float* xa,
+                                            const float* xb, float (&o)[4]) {
+  constexpr int CPG = 1 << LCPG;
+  constexpr int STEP = CPG < 2 ? 2 : CPG;
+  __syncwarp();
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3;
+  const int r = (lane & 7) + 8 * (mi & 1), dc = mi >> 1;
+  const uint32_t rbase = tile + (uint32_t)(r >> 3) * geo.half + (uint32_t)(r & 7) * geo.pitch;
+  o[0] = o[1] = o[2] = o[3] = 0.f;
+  auto fold = [&](const float (&v)[4], int gi) {
+    const uint32_t s0 = sb0[gi], s1 = sb1[gi];
+    const float XA = xa ? xa[gi] : 0.f, XB = xb ? xb[gi] : 0.f;
+    const float sc0 = bf16_lo(s0), sc1 = bf16_lo(s1);
+    const float bb0 = bf16_hi(s0) - 128.0f * sc0, bb1 = bf16_hi(s1) - 128.0f * sc1;
+    o[0] = fmaf(sc0, v[0], fmaf(bb0, XA, o[0]));
+    o[1] = fmaf(sc0, v[1], fmaf(bb0, XB, o[1]));
+    o[2] = fmaf(sc1, v[2], fmaf(bb1, XA, o[2]));
+    o[3] = fmaf(sc1, v[3], fmaf(bb1, XB, o[3]));
+  };
+#pragma unroll 2
+  for (int c = c0; c < c1; c += STEP) {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+    for (int cp = 0; cp < STEP; cp += 2) {
+      const int cc = c + cp + dc;
+      const uint32_t addr =
+          geo.swz ? rbase + (uint32_t)(cc >> 3) * geo.cb_stride + ((uint32_t)((cc & 7) ^ (r & 7)) << 4)
+                  : rbase + ((uint32_t)cc << 4);
+      uint32_t w[4];
+      ldsm_x4(addr, w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ch = c + cp + h;
+        uint4 b = make_uint4(0u, 0u, 0u, 0u);
+        if (b_src) b = __ldg(b_src + (size_t)ch * 4);
+        const uint32_t wg = w[2 * h], wg8 = w[2 * h + 1];
+        const uint32_t wg4 = wg >> 4, wg84 = wg8 >> 4;
+        mma16816(acc[2 * h], code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg4, 0),
+                 code_pair(wg84, 0), b.x, b.y);
+        mma16816(acc[2 * h + 1], code_pair(wg >> 8, 0), code_pair(wg8 >> 8, 0),
+                 code_pair(wg4 >> 8, 0), code_pair(wg84 >> 8, 0), b.z, b.w);
+        if (CPG == 1) {
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = acc[2 * h][i] + acc[2 * h + 1][i];
+          fold(v, ch);
+        }
+      }
+    }
+    if (CPG > 1) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+      fold(v, c >> LCPG);
+    }
+  }
+}
+
+// Gate/up + SwiGLU.  Units u = blockIdx.x + i * gridDim.x of (n_used + 1) *
+// (I / 8): expert index u / (I / 8) (the last one is the shared expert), tile
+// u % (I / 8) = pairs 8 tile .. 8 tile + 7 (interleaved rows 16 tile ..).
+// Thread 0 keeps kGuRing units in flight (TMA: two 8-row boxes and the
+// scales); the CTA's warps split a unit into (token tile, k-split) tasks.
+template <int NJ, int LCPG>
+__global__ void __launch_bounds__(kBThreads, 1) bdec_gateup_kernel(const BArgs a) {
+  constexpr int H = NJ * 256, NCB = H / 256, HC = H / 32;
+  constexpr int CPG = 1 << LCPG;
+  const int HG = H >> (LCPG + 5);
+  const int I = a.I, k = a.k, T = a.T, P = a.P;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.part + kBWarps * 16 * 8 * 4);
+  float* part = reinterpret_cast<float*>(sm + a.part);  // [task][16 rows][8 cols]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g4 = lane >> 2, tg = lane & 3;
+  const DecLayer* L = a.L;
+  const int n_slots = L->n_slots;
+  const int n_used = *a.n_used;
+  const int tpe = I / 8;  // units per expert
+  const int U = (n_used + 1) * tpe;
+  const int nu = (int)blockIdx.x < U ? (U - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const TileGeom geo{1024u, 128u, (uint32_t)NCB * 1024u, true};
+  if (tid == 0) {
+    for (int i = 0; i < kGuRing; ++i) ptx::mbar_init(&mbar[i], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int i) {  // thread 0: unit i of this CTA into slot i % kGuRing
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    const int ue = u / tpe, tile = u - ue * tpe;
+    const int s = i % kGuRing;
+    uint8_t* dst = sm + (size_t)s * a.gu_slot;
+    ptx::fence_proxy_async_smem();  // the slot's previous unit was read by ldmatrix
+    if (ue < n_used) {
+      const int slot = slot_of(a, a.used[ue], n_slots);
+      if (slot < 0) {
+        record_error(a.err, MOE_ERR_SLOT);
+        ptx::mbar_arrive_expect_tx(&mbar[s], 0);
+        return;
+      }
+      ptx::mbar_arrive_expect_tx(&mbar[s], (uint32_t)NCB * 2048 + 16u * HG * 4);
+      ptx::tma_load_4d(dst, &L->map_gu, 0, 16 * tile, 0, slot, &mbar[s]);
+      ptx::tma_load_4d(dst + NCB * 1024, &L->map_gu, 0, 16 * tile + 8, 0, slot, &mbar[s]);
+      ptx::bulk_g2s(dst + a.gu_sb, L->pool + (uint64_t)slot * L->stride + L->gu_sb +
+                                       (uint64_t)16 * tile * HG * 4,
+                    16u * HG * 4, &mbar[s]);
+    } else {
+      ptx::mbar_arrive_expect_tx(&mbar[s], (uint32_t)NCB * 2048 + 16u * HG * 4);
+      ptx::tma_load_4d(dst, &L->map_sgu, 0, 16 * tile, 0, 0, &mbar[s]);
+      ptx::tma_load_4d(dst + NCB * 1024, &L->map_sgu, 0, 16 * tile + 8, 0, 0, &mbar[s]);
+      ptx::bulk_g2s(dst + a.gu_sb, L->shared_blob + L->gu_sb + (uint64_t)16 * tile * HG * 4,
+                    16u * HG * 4, &mbar[s]);
+    }
+  };
+  if (tid == 0)
+    for (int i = 0; i < min(kGuRing, nu); ++i) issue(i);
+  for (int i = 0; i < nu; ++i) {
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    const int ue = u / tpe, tile = u - ue * tpe;
+    const int s = i % kGuRing;
+    const bool shared = ue >= n_used;
+    int pos0 = 0, n_e = T, hrow0 = P;
+    bool ok = true;
+    if (!shared) {
+      const int e = a.used[ue];
+      pos0 = a.offsets[e];
+      n_e = min(a.offsets[e + 1] - pos0, kBMaxT);
+      hrow0 = pos0;
+      ok = slot_of(a, e, n_slots) >= 0;
+    }
+    wait_bar(&mbar[s], (uint32_t)(i / kGuRing) & 1u, a.err);
+    const int ntiles = (n_e + 7) >> 3;
+    int kspl = ntiles == 1 ? 8 : ntiles == 2 ? 4 : ntiles <= 4 ? 2 : 1;
+    while (kspl > 1 && HC / kspl < (CPG < 2 ? 2 : CPG)) kspl >>= 1;
+    const int ntask = ntiles * kspl, span = HC / kspl;
+    const uint32_t tile_addr = ptx::smem_u32(sm + (size_t)s * a.gu_slot);
+    const uint32_t* sb = reinterpret_cast<const uint32_t*>(sm + (size_t)s * a.gu_slot + a.gu_sb);
+    for (int task = warp; task < ntask; task += kBWarps) {
+      const int nt = task / kspl, ks = task - nt * kspl;
+      auto token = [&](int idx) {
+        return idx < n_e ? (shared ? idx : a.perm[pos0 + idx] / k) : -1;
+      };
+      const int tb = token(nt * 8 + g4);
+      const int ta = token(nt * 8 + 2 * tg), tc = token(nt * 8 + 2 * tg + 1);
+      const uint4* b_src =
+          (ok && tb >= 0) ? reinterpret_cast<const uint4*>(a.xperm + (size_t)tb * H) + tg : nullptr;
+      float o[4];
+      tile_task_n<LCPG>(tile_addr, geo, ks * span, (ks + 1) * span, b_src, sb + g4 * HG,
+                        sb + (g4 + 8) * HG, ta >= 0 ? a.xg + (size_t)ta * HG : nullptr,
+                        tc >= 0 ? a.xg + (size_t)tc * HG : nullptr, o);
+      float* pt = part + (size_t)task * 128;
+      pt[g4 * 8 + 2 * tg] = o[0];
+      pt[g4 * 8 + 2 * tg + 1] = o[1];
+      pt[(g4 + 8) * 8 + 2 * tg] = o[2];
+      pt[(g4 + 8) * 8 + 2 * tg + 1] = o[3];
+    }
+    __syncthreads();
+    // SwiGLU of the unit's 8 pairs for each token, k-splits summed in order;
+    // one 16-byte entry of h per token: pairs (0, 4), (1, 5), (2, 6), (3, 7)
+    if (tid < n_e) {
+      const int nt = tid >> 3, col = tid & 7;
+      float hv[8];
+      float s8 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float gsum = 0.f, usum = 0.f;
+        for (int ks = 0; ks < kspl; ++ks) {
+          const float* pt = part + (size_t)(nt * kspl + ks) * 128;
+          gsum += pt[(2 * q) * 8 + col];
+          usum += pt[(2 * q + 1) * 8 + col];
+        }
+        hv[q] = ok ? silu_f(gsum) * usum : 0.f;
+      }
+      uint32_t hb[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        hb[q] = f32_to_bf16_rne(hv[q]);
+        s8 += __uint_as_float(hb[q] << 16);
+      }
+      const size_t row = (size_t)hrow0 + tid;
+      const int i0 = 8 * tile;  // first h index of the unit
+      uint4* dst = reinterpret_cast<uint4*>(a.hperm + row * I) + (i0 >> 5) * 4 + ((i0 & 31) >> 3);
+      *dst = make_uint4(hb[0] | (hb[4] << 16), hb[1] | (hb[5] << 16), hb[2] | (hb[6] << 16),
+                        hb[3] | (hb[7] << 16));
+      a.hs8[row * (I / 8) + tile] = s8;
+    }
+    __syncthreads();
+    if (tid == 0 && i + kGuRing < nu) issue(i + kGuRing);
+  }
+}
+
+// Down + combine.  CTA c owns rows 16 c .. 16 c + 15 of y.  The used experts
+// (and the shared one, last) come in batches of kDnBatch: thread 0 keeps two
+// batches of 16-row down tiles in flight; the warps take (expert, token tile)
+// tasks and leave each pair's 16 outputs in shared memory; then every token's
+// rows are combined in the order of its top-k, the gated shared expert last.
+template <int LCPG>
+__global__ void __launch_bounds__(kBThreads, 1) bdec_down_kernel(const BArgs a, int H) {
+  const int I = a.I, k = a.k, T = a.T, P = a.P;
+  const int IG = I >> (LCPG + 5), IC = I / 32;
+  const bool dswz = I / 2 >= 128;
+  const uint32_t pitch = dswz ? 128u : (uint32_t)(I / 2);
+  const int ncbd = dswz ? I / 256 : 1;
+  const TileGeom geo{16u * pitch, pitch, 8u * pitch, dswz};
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
+  float* oc = reinterpret_cast<float*>(sm + a.ocache);  // [P + T][16]
+  uint64_t* mbar =
+      reinterpret_cast<uint64_t*>(sm + a.ocache + (((size_t)(P + T) * 64 + 15) & ~size_t(15)));
+  __shared__ int s_first[kDnBatch + 1];  // first task of each expert of the batch
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g4 = lane >> 2, tg = lane & 3;
+  const DecLayer* L = a.L;
+  const int n_slots = L->n_slots;
+  const int r0 = 16 * (int)blockIdx.x;
+  const int n_used = *a.n_used;
+  const int nexp = n_used + 1;
+  const int nb = (nexp + kDnBatch - 1) / kDnBatch;
+  const uint32_t tile_bytes = (uint32_t)ncbd * 16 * pitch;
+  if (tid == 0) {
+    for (int i = 0; i < 2 * kDnBatch; ++i) ptx::mbar_init(&mbar[i], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // per expert of the list: its pairs (positions in perm) or the shared expert's tokens
+  auto expert = [&](int ue, int& pos0, int& n_e, int& hrow0, bool& ok) {
+    if (ue < n_used) {
+      const int e = a.used[ue];
+      pos0 = a.offsets[e];
+      n_e = min(a.offsets[e + 1] - pos0, kBMaxT);
+      hrow0 = pos0;
+      ok = slot_of(a, e, n_slots) >= 0;
+    } else {
+      pos0 = 0;
+      n_e = T;
+      hrow0 = P;
+      ok = true;
+    }
+  };
+  auto issue_batch = [&](int b) {  // thread 0
+    ptx::fence_proxy_async_smem();  // the slots' previous tiles were read by ldmatrix
+    for (int j = 0; j < kDnBatch; ++j) {
+      const int ue = b * kDnBatch + j;
+      if (ue >= nexp) break;
+      const int s = (b & 1) * kDnBatch + j;
+      uint8_t* dst = sm + (size_t)s * a.dn_slot;
+      if (ue < n_used) {
+        const int slot = slot_of(a, a.used[ue], n_slots);
+        if (slot < 0) {
+          record_error(a.err, MOE_ERR_SLOT);
+          ptx::mbar_arrive_expect_tx(&mbar[s], 0);
+          continue;
+        }
+        ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
+        ptx::tma_load_4d(dst, &L->map_d, 0, r0, 0, slot, &mbar[s]);
+        ptx::bulk_g2s(dst + a.dn_sb,
+                      L->pool + (uint64_t)slot * L->stride + L->d_sb + (uint64_t)r0 * IG * 4,
+                      16u * IG * 4, &mbar[s]);
+      } else {
+        ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
+        ptx::tma_load_4d(dst, &L->map_sd, 0, r0, 0, 0, &mbar[s]);
+        ptx::bulk_g2s(dst + a.dn_sb, L->shared_blob + L->d_sb + (uint64_t)r0 * IG * 4,
+                      16u * IG * 4, &mbar[s]);
+      }
+    }
+  };
+  if (tid == 0) {
+    issue_batch(0);
+    if (nb > 1) issue_batch(1);
+  }
+  for (int b = 0; b < nb; ++b) {
+    if (tid == 0) {
+      int acc = 0;
+      for (int j = 0; j < kDnBatch; ++j) {
+        s_first[j] = acc;
+        const int ue = b * kDnBatch + j;
+        if (ue < nexp) {
+          int pos0, n_e, hrow0;
+          bool ok;
+          expert(ue, pos0, n_e, hrow0, ok);
+          acc += (n_e + 7) >> 3;
+        }
+      }
+      s_first[kDnBatch] = acc;
+    }
+    __syncthreads();
+    const int ntask = s_first[kDnBatch];
+    for (int task = warp; task < ntask; task += kBWarps) {
+      int j = 0;
+      while (j + 1 < kDnBatch && s_first[j + 1] <= task) ++j;
+      const int nt = task - s_first[j];
+      const int ue = b * kDnBatch + j, s = (b & 1) * kDnBatch + j;
+      int pos0, n_e, hrow0;
+      bool ok;
+      expert(ue, pos0, n_e, hrow0, ok);
+      wait_bar(&mbar[s], (uint32_t)(b >> 1) & 1u, a.err);
+      const int ib = nt * 8 + g4, ia = nt * 8 + 2 * tg, ic = ia + 1;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      if (ok) {
+        const uint32_t* sb =
+            reinterpret_cast<const uint32_t*>(sm + (size_t)s * a.dn_slot + a.dn_sb);
+        const uint4* b_src =
+            ib < n_e ? reinterpret_cast<const uint4*>(a.hperm + (size_t)(hrow0 + ib) * I) + tg
+                     : nullptr;
+        tile_task_n<LCPG>(ptx::smem_u32(sm + (size_t)s * a.dn_slot), geo, 0, IC, b_src,
+                          sb + g4 * IG, sb + (g4 + 8) * IG,
+                          ia < n_e ? a.hg + (size_t)(hrow0 + ia) * IG : nullptr,
+                          ic < n_e ? a.hg + (size_t)(hrow0 + ic) * IG : nullptr, o);
+      }
+      if (ia < n_e) {
+        oc[(size_t)(hrow0 + ia) * 16 + g4] = o[0];
+        oc[(size_t)(hrow0 + ia) * 16 + g4 + 8] = o[2];
+      }
+      if (ic < n_e) {
+        oc[(size_t)(hrow0 + ic) * 16 + g4] = o[1];
+        oc[(size_t)(hrow0 + ic) * 16 + g4 + 8] = o[3];
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && b + 2 < nb) issue_batch(b + 2);
+  }
+  // combine: rows 2 q and 2 q + 1 of token t per thread
+  for (int w = tid; w < T * 8; w += kBThreads) {
+    const int t = w >> 3, q = w & 7;
+    float yv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = 2 * q + h;
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int pos = a.inv[t * k + j];
+        acc = fmaf(a.topk_w[t * k + j], oc[(size_t)pos * 16 + m], acc);
+      }
+      yv[h] = fmaf(a.gate[t], oc[(size_t)(P + t) * 16 + m], acc);
+    }
+    reinterpret_cast<uint32_t*>(a.y + (size_t)t * H + r0)[q] =
+        (uint32_t)f32_to_bf16_rne(yv[0]) | ((uint32_t)f32_to_bf16_rne(yv[1]) << 16);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------- routing
+// Router logits of T tokens in one launch: CTA c takes its share of the E
+// router rows (and CTA 0 the shared gate vector as one more row), staged in
+// shared memory; warp w takes tokens w, w + 8, ...  A lane sums each 8-element
+// chunk with 8 sequential FMAs and its chunks in order, a butterfly sums the
+// lanes, the prior comes last: depth D = 8 + H/256 + 5 + 1, so one uniform
+// bound per token, 2 D u (|x_t| max_e |Wr_e| + max|prior|) (Higham, Accuracy
+// and Stability of Numerical Algorithms, Thm. 4.3, with Cauchy-Schwarz),
+// covers every logit of the token.
+template <int NJ>
+__global__ void __launch_bounds__(256) bdec_router_kernel(
+    const uint16_t* __restrict__ x, int T, const uint16_t* __restrict__ rw,
+    const float* __restrict__ prior, const uint16_t* __restrict__ wsg, int E, float wmax,
+    float pmax, float* __restrict__ logits, float* __restrict__ beta, float* __restrict__ gate_z) {
+  constexpr int H = NJ * 256;
+  extern __shared__ uint8_t sm_raw[];
+  uint4* rows = reinterpret_cast<uint4*>(sm_raw);  // [nr (+1)][H/8]
+  const int nC = gridDim.x, c = blockIdx.x;
+  const int re0 = (int)(((long long)E * c) / nC), re1 = (int)(((long long)E * (c + 1)) / nC);
+  const int nr = re1 - re0, nrow = nr + (c == 0 ? 1 : 0);
+  for (int i = threadIdx.x; i < nrow * (H / 8); i += blockDim.x) {
+    const int r = i / (H / 8), j = i - r * (H / 8);
+    const uint16_t* src = r < nr ? rw + (size_t)(re0 + r) * H : wsg;
+    rows[i] = __ldg(reinterpret_cast<const uint4*>(src) + j);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int DEPTH = 8 + NJ + 5 + 1;
+  for (int t = warp; t < T; t += blockDim.x >> 5) {
+    uint4 xv[NJ];
+    float ss = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+      xv[jj] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + lane + 32 * jj);
+      const uint32_t w4[4] = {xv[jj].x, xv[jj].y, xv[jj].z, xv[jj].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        ss = fmaf(bf16_lo(w4[q]), bf16_lo(w4[q]), fmaf(bf16_hi(w4[q]), bf16_hi(w4[q]), ss));
+    }
+    for (int r = 0; r < nrow; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const uint4 wv = rows[(size_t)r * (H / 8) + lane + 32 * jj];
+        const uint32_t a4[4] = {xv[jj].x, xv[jj].y, xv[jj].z, xv[jj].w};
+        const uint32_t b4[4] = {wv.x, wv.y, wv.z, wv.w};
+        float sc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          sc = fmaf(bf16_lo(a4[q]), bf16_lo(b4[q]), sc);
+          sc = fmaf(bf16_hi(a4[q]), bf16_hi(b4[q]), sc);
+        }
+        acc += sc;
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) {
+        if (r < nr)
+          logits[(size_t)t * E + re0 + r] = acc + (prior ? prior[re0 + r] : 0.f);
+        else
+          gate_z[t] = acc;
+      }
+    }
+    if (c == 0) {
+      ss = warp_sum(ss);
+      // |x_t| rounded up (the fp32 sum of squares is within H u of the exact one)
+      const float X = sqrtf(ss * 1.0009765625f) * 1.0009765625f;
+      if (lane == 0)
+        beta[t] = 2.0f * (float)DEPTH * 5.9604644775390625e-8f * 1.01f * (X * wmax + pmax) +
+                  rt::kBoundFloor;
+    }
+  }
+}
+
+// Logits of one token with one uniform bound, for the exact selection routine.
+struct TokenLogits {
+  const float* l;
+  float b;
+  __device__ __forceinline__ void get(int e, float& logit, float& bnd) const {
+    logit = __ldcg(l + e);
+    bnd = b;
+  }
+  __device__ __forceinline__ int id(int e) const { return e; }
+};
+
+// Exact top-k of token blockIdx.x (the CTA-wide routine of routing_common.cuh),
+// renormalised weights and the shared gate.
+__global__ void __launch_bounds__(256) bdec_select_kernel(
+    const float* __restrict__ logits, const float* __restrict__ beta,
+    const float* __restrict__ gate_z, const uint16_t* __restrict__ x,
+    const uint16_t* __restrict__ rw, const float* __restrict__ prior, int E, int k, int H,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, float* __restrict__ gate) {
+  constexpr int V = kMaxE / 256;
+  extern __shared__ uint8_t sm_raw[];
+  const int t = blockIdx.x;
+  const size_t sel = (rt::topk_warp_smem(E) + 15) & ~size_t(15);
+  int* si;
+  float* sv;
+  rt::topk_select_block<V>(TokenLogits{logits + (size_t)t * E, beta[t]}, E, k, x + (size_t)t * H,
+                           rw, prior, H, sm_raw, reinterpret_cast<uint2*>(sm_raw + sel),
+                           reinterpret_cast<float*>(sm_raw + sel + 256 * V * 8), &si, &sv);
+  if (threadIdx.x < 32) {
+    const float w = rt::renormalised_weight(sv, k);
+    const int lane = threadIdx.x;
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = si[lane];
+      topk_w[(size_t)t * k + lane] = w;
+    }
+    if (lane == 0) gate[t] = 1.0f / (1.0f + __expf(-gate_z[t]));
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+// ---------------------------------------------------------------- host side
+namespace moe {
+namespace {
+
+uint32_t up_u32(uint64_t v, uint64_t al) { return (uint32_t)((v + al - 1) / al * al); }
+
+struct BPlan {
+  uint32_t gu_slot, gu_sb, part, smem_gu, dn_slot, dn_sb, ocache, smem_dn;
+};
+
+bool bplan(const Dims& d, int T, BPlan& p) {
+  const int H = d.H, I = d.I, G = d.G;
+  const int NCB = H / 256, HG = H / G, IG = I / G;
+  const bool dswz = I / 2 >= 128;
+  const uint64_t pitch = dswz ? 128 : (uint64_t)(I / 2);
+  const uint64_t ncbd = dswz ? (uint64_t)(I / 256) : 1;
+  p.gu_sb = (uint32_t)NCB * 2048;
+  p.gu_slot = up_u32((uint64_t)p.gu_sb + 16ull * HG * 4, 1024);
+  p.part = kGuRing * p.gu_slot;
+  p.smem_gu = p.part + kBWarps * 16 * 8 * 4 + kGuRing * 8 + 1024;
+  p.dn_sb = up_u32(ncbd * 16 * pitch, 128);
+  p.dn_slot = up_u32((uint64_t)p.dn_sb + 16ull * IG * 4, 1024);
+  p.ocache = 2 * kDnBatch * p.dn_slot;
+  const uint64_t rows = (uint64_t)T * d.k + T;
+  p.smem_dn = (uint32_t)(p.ocache + ((rows * 64 + 15) & ~15ull) + 2 * kDnBatch * 8 + 1024);
+  return T >= 2 && T <= kBMaxT && decode_shape_ok(d) && p.smem_gu <= kBSmemMax &&
+         p.smem_dn <= kBSmemMax;
+}
+
+template <int NJ, int LC>
+struct GateUpF {
+  static cudaError_t attr() {
+    return cudaFuncSetAttribute(bdec_gateup_kernel<NJ, LC>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemMax);
+  }
+  static cudaError_t run(const BArgs* a, int nC, cudaStream_t st) {
+    bdec_gateup_kernel<NJ, LC><<<nC, kBThreads, a->smem_gu, st>>>(*a);
+    return cudaGetLastError();
+  }
+};
+
+template <int LC>
+cudaError_t down_run(const BArgs& a, int H, cudaStream_t st) {
+  bdec_down_kernel<LC><<<H / 16, kBThreads, a.smem_dn, st>>>(a, H);
+  return cudaGetLastError();
+}
+
+template <int NJ>
+cudaError_t gu_dispatch_lc(int lc, bool attr_only, const BArgs* a, int nC, cudaStream_t st) {
+  if (lc == 0) return attr_only ? GateUpF<NJ, 0>::attr() : GateUpF<NJ, 0>::run(a, nC, st);
+  if (lc == 1) return attr_only ? GateUpF<NJ, 1>::attr() : GateUpF<NJ, 1>::run(a, nC, st);
+  return attr_only ? GateUpF<NJ, 2>::attr() : GateUpF<NJ, 2>::run(a, nC, st);
+}
+
+cudaError_t gu_dispatch(const Dims& d, bool attr_only, const BArgs* a, int nC, cudaStream_t st) {
+  const int lc = d.G == 32 ? 0 : d.G == 64 ? 1 : 2;
+  switch (d.H / 256) {
+    case 1: return gu_dispatch_lc<1>(lc, attr_only, a, nC, st);
+    case 2: return gu_dispatch_lc<2>(lc, attr_only, a, nC, st);
+    case 4: return gu_dispatch_lc<4>(lc, attr_only, a, nC, st);
+    case 8: return gu_dispatch_lc<8>(lc, attr_only, a, nC, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool batch_decode_supported(const Ctx& c, int T) {
+  BPlan p;
+  return c.dec_ok && c.dec_layer && !c.pl.slots && bplan(c.d, T, p);
+}
+
+cudaError_t prepare_batch_decode(const Ctx& c) {
+  BPlan p;
+  if (!c.dec_ok || !bplan(c.d, 2, p)) return cudaSuccess;
+  cudaError_t e = gu_dispatch(c.d, true, nullptr, 0, nullptr);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bdec_down_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBSmemMax);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bdec_down_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBSmemMax);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bdec_down_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBSmemMax);
+  return e;
+}
+
+cudaError_t launch_batch_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches) {
+  const Dims& d = c.d;
+  const int T = f.T, E = d.E, H = d.H, nC = c.num_sms;
+  const size_t rsm = (size_t)(E / nC + 2) * H * 2;
+  float* beta = c.ws.bound;  // [T]: one bound per token
+#define MOE_BDR(NJ)                                                                            \
+  bdec_router_kernel<NJ><<<nC, 256, rsm, st>>>(f.x, T, c.router_w, c.router_bias,             \
+                                                c.shared_gate_w, E, c.dec_wmax, c.dec_pmax,   \
+                                                c.ws.logits, beta, c.ws.gate_z)
+  switch (H / 256) {
+    case 1: MOE_BDR(1); break;
+    case 2: MOE_BDR(2); break;
+    case 4: MOE_BDR(4); break;
+    case 8: MOE_BDR(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_BDR
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t ssm = ((rt::topk_warp_smem(E) + 15) & ~size_t(15)) + 256 * (kMaxE / 256) * 8 + 64;
+  bdec_select_kernel<<<T, 256, ssm, st>>>(c.ws.logits, beta, c.ws.gate_z, f.x, c.router_w,
+                                           c.router_bias, E, d.k, H, f.topk_idx, f.topk_w,
+                                           c.ws.gate);
+  *launches += 2;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_batch_decode(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches) {
+  const Dims& d = c.d;
+  BPlan p;
+  if (!bplan(d, f.T, p)) return cudaErrorInvalidValue;
+  const int T = f.T, H = d.H, I = d.I, G = d.G, P = T * d.k;
+  BArgs a{};
+  a.L = c.dec_layer;
+  a.T = T;
+  a.k = d.k;
+  a.E = d.E;
+  a.I = I;
+  a.G = G;
+  a.P = P;
+  a.used = c.ws.used;
+  a.n_used = c.ws.n_used;
+  a.offsets = c.ws.offsets;
+  a.perm = c.ws.perm;
+  a.inv = c.ws.inv;
+  a.table = f.table;
+  a.x = f.x;
+  // scratch: h in the workspace's h rows, the rest in its fp32 output rows
+  a.hperm = reinterpret_cast<uint16_t*>(c.ws.h);
+  uint8_t* o = reinterpret_cast<uint8_t*>(c.ws.o);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = o + off;
+    off += (bytes + 255) & ~size_t(255);
+    return r;
+  };
+  a.xperm = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
+  a.xg = reinterpret_cast<float*>(take((size_t)T * (H / G) * 4));
+  a.hs8 = reinterpret_cast<float*>(take((size_t)(P + T) * (I / 8) * 4));
+  a.hg = reinterpret_cast<float*>(take((size_t)(P + T) * (I / G) * 4));
+  a.topk_w = f.topk_w;
+  a.gate = c.ws.gate;
+  a.y = f.y;
+  a.err = c.err;
+  a.gu_slot = p.gu_slot;
+  a.gu_sb = p.gu_sb;
+  a.part = p.part;
+  a.smem_gu = p.smem_gu;
+  a.dn_slot = p.dn_slot;
+  a.dn_sb = p.dn_sb;
+  a.ocache = p.ocache;
+  a.smem_dn = p.smem_dn;
+  bdec_prep_kernel<<<T, 256, 0, st>>>(f.x, H, G, a.xperm, a.xg);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = gu_dispatch(d, false, &a, c.num_sms, st);
+  if (e == cudaSuccess) {
+    const int n = (P + T) * (I / G);
+    bdec_hsum_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.hs8, P + T, I, G, a.hg);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    const int lc = G == 32 ? 0 : G == 64 ? 1 : 2;
+    e = lc == 0 ? down_run<0>(a, H, st) : lc == 1 ? down_run<1>(a, H, st) : down_run<2>(a, H, st);
+  }
+  *launches += 4;
+  return e;
+}
+
+}  // namespace moe

@@ -170,6 +170,12 @@ cudaError_t launch_unpack_expert(const uint8_t* blob, int H, int I, int G, const
 
 cudaError_t launch_pool_update(const Ctx& c, const int32_t* topk_idx, int P, cudaStream_t st,
                                int* launches);
+struct FwdArgs;
+// Batched decode (batch_decode.cu): 2 <= T <= 64 tokens, after routing and the permutation.
+bool batch_decode_supported(const Ctx& c, int T);
+cudaError_t prepare_batch_decode(const Ctx& c);
+cudaError_t launch_batch_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches);
+cudaError_t launch_batch_decode(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches);
 
 struct FwdArgs {
   const uint16_t* x;
