@@ -29,8 +29,6 @@ using namespace mmag;
 
 constexpr int kBThreads = 256;
 constexpr int kBWarps = 8;
-constexpr int kGuRing = 4;    // gate/up unit slots
-constexpr int kDnBatch = 8;   // down: experts per batch, two batches in flight
 constexpr int kBMaxT = 64;
 // dynamic shared memory limit of these kernels (the down kernel also has a
 // little static shared memory; the sum must stay within the device's 227 KB)
@@ -55,8 +53,8 @@ struct BArgs {
   const float* gate;       // [T] shared-expert gate
   uint16_t* y;             // [T][H]
   int32_t* err;
-  uint32_t gu_slot, gu_sb, part;       // gate/up shared-memory plan (byte offsets)
-  uint32_t dn_slot, dn_sb, ocache;     // down shared-memory plan
+  uint32_t gu_slot, gu_sb, part;       // gate/up: part slot bytes, scale buffer bytes, barriers
+  uint32_t dn_slot, dn_sb, ocache;     // down: slot bytes, scales within a slot, outputs
   uint32_t smem_gu, smem_dn;
 };
 
@@ -113,41 +111,49 @@ __global__ void __launch_bounds__(256) bdec_hsum_kernel(const float* __restrict_
   hg[i] = s;
 }
 
-// One task: chunks [c0, c1) of K of a 16-row tile against 8 token columns.
-// Lane (g = lane / 4, t = lane % 4) loads column g's input (b_src, or zeros
-// when null) and ends with rows g, g + 8 x columns 2t, 2t + 1 in o[0..3]
-// (row g col 2t, row g col 2t+1, row g+8 col 2t, row g+8 col 2t+1).
-//   b_src    this lane's column: 16-byte entries (chunk, t) 64 bytes apart
-//   sb0/1    (scale | bias << 16) words of rows g and g + 8, one per group
-//   xa, xb   group sums of columns 2t and 2t + 1 (null: column unused)
-template <int LCPG>
-__device__ __forceinline__ void tile_task_n(uint32_t tile, TileGeom geo, int c0, int c1,
-                                            const uint4* b_src, const uint32_t* sb0,
-                                            const uint32_t* sb1, const float* xa,
-                                            const float* xb, float (&o)[4]) {
+// Chunks [c0, c1) of a 16-row tile (local chunk indices; the tile's first
+// chunk is chunk cg of the row) against NT tiles of 8 input columns at once:
+// the weights' fragments are loaded and converted once per chunk pair and
+// serve every column tile.  Lane (g = lane / 4, t = lane % 4) loads column g
+// of each tile (input row tb[nt], or zeros when negative) and accumulates
+// rows g, g + 8 x columns 2t, 2t + 1 into o[nt][0..3] (row g col 2t, row g
+// col 2t + 1, row g + 8 col 2t, row g + 8 col 2t + 1), folding each group as
+//   sum_c (s q_c + b) x_c = s sum_c (128 + q_c) x_c + (b - 128 s) sum_c x_c.
+//   src, row_elems  the input rows (bf16, k-permuted) and their stride
+//   ta, tc          input rows of columns 2t, 2t + 1 (negative: unused)
+//   sb0/1           (scale | bias << 16) words of rows g and g + 8, per group
+//   xg, ng          per-row group sums of the input rows, ng per row
+template <int LCPG, int NT>
+__device__ __forceinline__ void tile_mn(uint32_t tile, TileGeom geo, int c0, int c1, int cg,
+                                        const uint16_t* src, int row_elems, const int (&tb)[NT],
+                                        const int (&ta)[NT], const int (&tc)[NT],
+                                        const uint32_t* sb0, const uint32_t* sb1,
+                                        const float* xg, int ng, float (&o)[NT][4]) {
   constexpr int CPG = 1 << LCPG;
   constexpr int STEP = CPG < 2 ? 2 : CPG;
-  __syncwarp();
   const int lane = threadIdx.x & 31;
   const int mi = lane >> 3;
   const int r = (lane & 7) + 8 * (mi & 1), dc = mi >> 1;
+  const int tg = lane & 3;
   const uint32_t rbase = tile + (uint32_t)(r >> 3) * geo.half + (uint32_t)(r & 7) * geo.pitch;
-  o[0] = o[1] = o[2] = o[3] = 0.f;
-  auto fold = [&](const float (&v)[4], int gi) {
+  auto fold = [&](const float (&acc)[NT][4], int gi) {
     const uint32_t s0 = sb0[gi], s1 = sb1[gi];
-    const float XA = xa ? xa[gi] : 0.f, XB = xb ? xb[gi] : 0.f;
     const float sc0 = bf16_lo(s0), sc1 = bf16_lo(s1);
     const float bb0 = bf16_hi(s0) - 128.0f * sc0, bb1 = bf16_hi(s1) - 128.0f * sc1;
-    o[0] = fmaf(sc0, v[0], fmaf(bb0, XA, o[0]));
-    o[1] = fmaf(sc0, v[1], fmaf(bb0, XB, o[1]));
-    o[2] = fmaf(sc1, v[2], fmaf(bb1, XA, o[2]));
-    o[3] = fmaf(sc1, v[3], fmaf(bb1, XB, o[3]));
-  };
-#pragma unroll 2
-  for (int c = c0; c < c1; c += STEP) {
-    float acc[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      const float XA = ta[nt] >= 0 ? xg[(size_t)ta[nt] * ng + gi] : 0.f;
+      const float XB = tc[nt] >= 0 ? xg[(size_t)tc[nt] * ng + gi] : 0.f;
+      o[nt][0] = fmaf(sc0, acc[nt][0], fmaf(bb0, XA, o[nt][0]));
+      o[nt][1] = fmaf(sc0, acc[nt][1], fmaf(bb0, XB, o[nt][1]));
+      o[nt][2] = fmaf(sc1, acc[nt][2], fmaf(bb1, XA, o[nt][2]));
+      o[nt][3] = fmaf(sc1, acc[nt][3], fmaf(bb1, XB, o[nt][3]));
+    }
+  };
+  for (int c = c0; c < c1; c += STEP) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
     for (int cp = 0; cp < STEP; cp += 2) {
       const int cc = c + cp + dc;
@@ -158,174 +164,268 @@ __device__ __forceinline__ void tile_task_n(uint32_t tile, TileGeom geo, int c0,
       ldsm_x4(addr, w[0], w[1], w[2], w[3]);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int ch = c + cp + h;
-        uint4 b = make_uint4(0u, 0u, 0u, 0u);
-        if (b_src) b = __ldg(b_src + (size_t)ch * 4);
+        const int chg = cg + c + cp + h;  // chunk of the row
         const uint32_t wg = w[2 * h], wg8 = w[2 * h + 1];
         const uint32_t wg4 = wg >> 4, wg84 = wg8 >> 4;
-        mma16816(acc[2 * h], code_pair(wg, 0), code_pair(wg8, 0), code_pair(wg4, 0),
-                 code_pair(wg84, 0), b.x, b.y);
-        mma16816(acc[2 * h + 1], code_pair(wg >> 8, 0), code_pair(wg8 >> 8, 0),
-                 code_pair(wg4 >> 8, 0), code_pair(wg84 >> 8, 0), b.z, b.w);
-        if (CPG == 1) {
-          float v[4];
+        const uint32_t a0 = code_pair(wg, 0), a1 = code_pair(wg8, 0), a2 = code_pair(wg4, 0),
+                       a3 = code_pair(wg84, 0);
+        const uint32_t a4 = code_pair(wg >> 8, 0), a5 = code_pair(wg8 >> 8, 0),
+                       a6 = code_pair(wg4 >> 8, 0), a7 = code_pair(wg84 >> 8, 0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) v[i] = acc[2 * h][i] + acc[2 * h + 1][i];
-          fold(v, ch);
+        for (int nt = 0; nt < NT; ++nt) {
+          uint4 b = make_uint4(0u, 0u, 0u, 0u);
+          if (tb[nt] >= 0)
+            b = __ldg(reinterpret_cast<const uint4*>(src + (size_t)tb[nt] * row_elems) +
+                      (size_t)chg * 4 + tg);
+          mma16816(acc[nt], a0, a1, a2, a3, b.x, b.y);
+          mma16816(acc[nt], a4, a5, a6, a7, b.z, b.w);
+        }
+        if (CPG == 1) {
+          fold(acc, chg);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         }
       }
     }
-    if (CPG > 1) {
-      float v[4];
+    if (CPG > 1) fold(acc, (cg + c) >> LCPG);
+  }
+}
+
+// The unit list: u / (I / 8) indexes the used experts (the last one is the
+// shared expert), u % (I / 8) is a tile of 8 gate/up pairs (16 rows).
+struct UnitInfo {
+  int tile, pos0, n_e, hrow0, slot;  // slot: -1 missing, -2 the shared expert
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const BArgs& a, int u, int n_used, int n_slots) {
+  const int tpe = a.I / 8;
+  const int ue = u / tpe;
+  UnitInfo U;
+  U.tile = u - ue * tpe;
+  if (ue < n_used) {
+    const int e = a.used[ue];
+    U.pos0 = a.offsets[e];
+    U.n_e = min(a.offsets[e + 1] - U.pos0, kBMaxT);
+    U.hrow0 = U.pos0;
+    U.slot = slot_of(a, e, n_slots);
+  } else {
+    U.pos0 = 0;
+    U.n_e = a.T;
+    U.hrow0 = a.P;
+    U.slot = -2;
+  }
+  return U;
+}
+
+// Gate/up + SwiGLU.  This CTA's units u = blockIdx.x + i * gridDim.x go to
+// its warps round robin (i = w, w + 8, ...); each warp streams its units in
+// NH parts (halves of the rows when a row holds 2 column blocks or more)
+// through two slots of its own, with every token tile of the unit's expert
+// at once, and writes h itself: no CTA-wide barrier.
+template <int NJ, int LCPG, int NT>
+__device__ __forceinline__ void gu_unit_part(const BArgs& a, const UnitInfo& U, int part,
+                                             uint32_t tile, const uint32_t* sb, float (&o)[8][4]) {
+  constexpr int H = NJ * 256, NCB = H / 256, HC = H / 32;
+  constexpr int NH = NCB >= 2 ? 2 : 1, PHC = HC / NH;
+  const int HG = H >> (LCPG + 5);
+  const int lane = threadIdx.x & 31, g4 = lane >> 2, tg = lane & 3;
+  const TileGeom geo{1024u, 128u, (uint32_t)(NCB / NH) * 1024u, true};
+  const bool shared = U.slot == -2;
+  auto token = [&](int idx) {
+    return idx < U.n_e ? (shared ? idx : a.perm[U.pos0 + idx] / a.k) : -1;
+  };
+  int tb[NT], ta[NT], tc[NT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
-      fold(v, c >> LCPG);
+  for (int nt = 0; nt < NT; ++nt) {
+    tb[nt] = U.slot == -1 ? -1 : token(nt * 8 + g4);
+    ta[nt] = token(nt * 8 + 2 * tg);
+    tc[nt] = token(nt * 8 + 2 * tg + 1);
+  }
+  tile_mn<LCPG, NT>(tile, geo, 0, PHC, part * PHC, a.xperm, H, tb, ta, tc, sb + g4 * HG,
+                    sb + (g4 + 8) * HG, a.xg, HG, reinterpret_cast<float(&)[NT][4]>(o));
+}
+
+template <int NT>
+__device__ __forceinline__ void gu_epilogue(const BArgs& a, const UnitInfo& U, float (&o)[8][4]) {
+  const int I = a.I;
+  const int lane = threadIdx.x & 31, g4 = lane >> 2, tg = lane & 3;
+  const bool ok = U.slot != -1;
+  const int i0 = 8 * U.tile;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    // even g: gate rows 2m, 2m + 8 (pairs m, m + 4); lane + 4 holds their up rows
+    float up[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) up[i] = __shfl_down_sync(0xffffffffu, o[nt][i], 4);
+    float h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = ok ? silu_f(o[nt][i]) * up[i] : 0.f;
+    const uint32_t b0 = f32_to_bf16_rne(h[0]), b1 = f32_to_bf16_rne(h[1]);
+    const uint32_t b2 = f32_to_bf16_rne(h[2]), b3 = f32_to_bf16_rne(h[3]);
+    // the sum of the 8 values of each column: pairs (m, m + 4) over m = 0..3
+    float sa = __uint_as_float(b0 << 16) + __uint_as_float(b2 << 16);
+    float sc = __uint_as_float(b1 << 16) + __uint_as_float(b3 << 16);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 8);
+    sa += __shfl_xor_sync(0xffffffffu, sa, 16);
+    sc += __shfl_xor_sync(0xffffffffu, sc, 8);
+    sc += __shfl_xor_sync(0xffffffffu, sc, 16);
+    if ((g4 & 1) == 0) {
+      const int m = g4 >> 1;
+      const int ia = nt * 8 + 2 * tg, ic = ia + 1;
+      // word m of a column's 16-byte entry is the bf16 pair (h_m, h_m+4)
+      if (ia < U.n_e) {
+        const size_t row = (size_t)U.hrow0 + ia;
+        reinterpret_cast<uint32_t*>(a.hperm + row * I + (i0 >> 5) * 32 + ((i0 & 31) >> 3) * 8)[m] =
+            b0 | (b2 << 16);
+        if (m == 0) a.hs8[row * (I / 8) + U.tile] = sa;
+      }
+      if (ic < U.n_e) {
+        const size_t row = (size_t)U.hrow0 + ic;
+        reinterpret_cast<uint32_t*>(a.hperm + row * I + (i0 >> 5) * 32 + ((i0 & 31) >> 3) * 8)[m] =
+            b1 | (b3 << 16);
+        if (m == 0) a.hs8[row * (I / 8) + U.tile] = sc;
+      }
     }
   }
 }
 
-// Gate/up + SwiGLU.  Units u = blockIdx.x + i * gridDim.x of (n_used + 1) *
-// (I / 8): expert index u / (I / 8) (the last one is the shared expert), tile
-// u % (I / 8) = pairs 8 tile .. 8 tile + 7 (interleaved rows 16 tile ..).
-// Thread 0 keeps kGuRing units in flight (TMA: two 8-row boxes and the
-// scales); the CTA's warps split a unit into (token tile, k-split) tasks.
 template <int NJ, int LCPG>
 __global__ void __launch_bounds__(kBThreads, 1) bdec_gateup_kernel(const BArgs a) {
-  constexpr int H = NJ * 256, NCB = H / 256, HC = H / 32;
-  constexpr int CPG = 1 << LCPG;
+  constexpr int H = NJ * 256, NCB = H / 256;
+  constexpr int NH = NCB >= 2 ? 2 : 1, PCB = NCB / NH;
   const int HG = H >> (LCPG + 5);
-  const int I = a.I, k = a.k, T = a.T, P = a.P;
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.part + kBWarps * 16 * 8 * 4);
-  float* part = reinterpret_cast<float*>(sm + a.part);  // [task][16 rows][8 cols]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, tg = lane & 3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t pslot = (uint32_t)PCB * 2048;  // one part: 16 rows x PCB column blocks
+  uint8_t* slots = sm + (size_t)warp * 2 * pslot;
+  uint8_t* sbuf = sm + (size_t)kBWarps * 2 * pslot + (size_t)warp * 2 * a.gu_sb;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.part) + warp * 2;
   const DecLayer* L = a.L;
   const int n_slots = L->n_slots;
   const int n_used = *a.n_used;
-  const int tpe = I / 8;  // units per expert
-  const int U = (n_used + 1) * tpe;
-  const int nu = (int)blockIdx.x < U ? (U - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-  const TileGeom geo{1024u, 128u, (uint32_t)NCB * 1024u, true};
-  if (tid == 0) {
-    for (int i = 0; i < kGuRing; ++i) ptx::mbar_init(&mbar[i], 1);
+  const int U_all = (n_used + 1) * (a.I / 8);
+  const int nu = (int)blockIdx.x < U_all ?
+                 (U_all - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int nw = nu > warp ? (nu - warp + kBWarps - 1) / kBWarps : 0;  // this warp's units
+  const int nitems = nw * NH;
+  if (lane == 0) {
+    ptx::mbar_init(&mbar[0], 1);
+    ptx::mbar_init(&mbar[1], 1);
     ptx::fence_mbar_init();
   }
-  __syncthreads();
-  auto issue = [&](int i) {  // thread 0: unit i of this CTA into slot i % kGuRing
-    const int u = (int)blockIdx.x + i * (int)gridDim.x;
-    const int ue = u / tpe, tile = u - ue * tpe;
-    const int s = i % kGuRing;
-    uint8_t* dst = sm + (size_t)s * a.gu_slot;
-    ptx::fence_proxy_async_smem();  // the slot's previous unit was read by ldmatrix
-    if (ue < n_used) {
-      const int slot = slot_of(a, a.used[ue], n_slots);
-      if (slot < 0) {
-        record_error(a.err, MOE_ERR_SLOT);
-        ptx::mbar_arrive_expect_tx(&mbar[s], 0);
-        return;
-      }
-      ptx::mbar_arrive_expect_tx(&mbar[s], (uint32_t)NCB * 2048 + 16u * HG * 4);
-      ptx::tma_load_4d(dst, &L->map_gu, 0, 16 * tile, 0, slot, &mbar[s]);
-      ptx::tma_load_4d(dst + NCB * 1024, &L->map_gu, 0, 16 * tile + 8, 0, slot, &mbar[s]);
-      ptx::bulk_g2s(dst + a.gu_sb, L->pool + (uint64_t)slot * L->stride + L->gu_sb +
-                                       (uint64_t)16 * tile * HG * 4,
-                    16u * HG * 4, &mbar[s]);
-    } else {
-      ptx::mbar_arrive_expect_tx(&mbar[s], (uint32_t)NCB * 2048 + 16u * HG * 4);
-      ptx::tma_load_4d(dst, &L->map_sgu, 0, 16 * tile, 0, 0, &mbar[s]);
-      ptx::tma_load_4d(dst + NCB * 1024, &L->map_sgu, 0, 16 * tile + 8, 0, 0, &mbar[s]);
-      ptx::bulk_g2s(dst + a.gu_sb, L->shared_blob + L->gu_sb + (uint64_t)16 * tile * HG * 4,
-                    16u * HG * 4, &mbar[s]);
+  __syncwarp();
+  auto unit_of = [&](int q) {  // this warp's q-th item's unit index
+    return (int)blockIdx.x + (warp + kBWarps * (q / NH)) * (int)gridDim.x;
+  };
+  auto issue = [&](int q) {  // lane 0
+    const UnitInfo U = unit_info(a, unit_of(q), n_used, n_slots);
+    const int part = q % NH, s = q & 1;
+    uint8_t* dst = slots + (size_t)s * pslot;
+    uint8_t* sdst = sbuf + (size_t)((q / NH) & 1) * a.gu_sb;
+    ptx::fence_proxy_async_smem();  // the slot's previous part was read by ldmatrix
+    if (U.slot == -1) {
+      record_error(a.err, MOE_ERR_SLOT);
+      ptx::mbar_arrive_expect_tx(&mbar[s], 0);
+      return;
+    }
+    const bool shared = U.slot == -2;
+    const CUtensorMap* map = NH == 1 ? (shared ? &L->map_sgu : &L->map_gu)
+                                     : (shared ? &L->map_sguh : &L->map_guh);
+    const int sl = shared ? 0 : U.slot;
+    const uint32_t sbytes = part == 0 ? 16u * HG * 4 : 0u;
+    ptx::mbar_arrive_expect_tx(&mbar[s], pslot + sbytes);
+    ptx::tma_load_4d(dst, map, 0, 16 * U.tile, part * PCB, sl, &mbar[s]);
+    ptx::tma_load_4d(dst + PCB * 1024, map, 0, 16 * U.tile + 8, part * PCB, sl, &mbar[s]);
+    if (part == 0) {
+      const uint8_t* sb = shared ? L->shared_blob + L->gu_sb
+                                 : L->pool + (uint64_t)U.slot * L->stride + L->gu_sb;
+      ptx::bulk_g2s(sdst, sb + (uint64_t)16 * U.tile * HG * 4, sbytes, &mbar[s]);
     }
   };
-  if (tid == 0)
-    for (int i = 0; i < min(kGuRing, nu); ++i) issue(i);
-  for (int i = 0; i < nu; ++i) {
-    const int u = (int)blockIdx.x + i * (int)gridDim.x;
-    const int ue = u / tpe, tile = u - ue * tpe;
-    const int s = i % kGuRing;
-    const bool shared = ue >= n_used;
-    int pos0 = 0, n_e = T, hrow0 = P;
-    bool ok = true;
-    if (!shared) {
-      const int e = a.used[ue];
-      pos0 = a.offsets[e];
-      n_e = min(a.offsets[e + 1] - pos0, kBMaxT);
-      hrow0 = pos0;
-      ok = slot_of(a, e, n_slots) >= 0;
-    }
-    wait_bar(&mbar[s], (uint32_t)(i / kGuRing) & 1u, a.err);
-    const int ntiles = (n_e + 7) >> 3;
-    int kspl = ntiles == 1 ? 8 : ntiles == 2 ? 4 : ntiles <= 4 ? 2 : 1;
-    while (kspl > 1 && HC / kspl < (CPG < 2 ? 2 : CPG)) kspl >>= 1;
-    const int ntask = ntiles * kspl, span = HC / kspl;
-    const uint32_t tile_addr = ptx::smem_u32(sm + (size_t)s * a.gu_slot);
-    const uint32_t* sb = reinterpret_cast<const uint32_t*>(sm + (size_t)s * a.gu_slot + a.gu_sb);
-    for (int task = warp; task < ntask; task += kBWarps) {
-      const int nt = task / kspl, ks = task - nt * kspl;
-      auto token = [&](int idx) {
-        return idx < n_e ? (shared ? idx : a.perm[pos0 + idx] / k) : -1;
-      };
-      const int tb = token(nt * 8 + g4);
-      const int ta = token(nt * 8 + 2 * tg), tc = token(nt * 8 + 2 * tg + 1);
-      const uint4* b_src =
-          (ok && tb >= 0) ? reinterpret_cast<const uint4*>(a.xperm + (size_t)tb * H) + tg : nullptr;
-      float o[4];
-      tile_task_n<LCPG>(tile_addr, geo, ks * span, (ks + 1) * span, b_src, sb + g4 * HG,
-                        sb + (g4 + 8) * HG, ta >= 0 ? a.xg + (size_t)ta * HG : nullptr,
-                        tc >= 0 ? a.xg + (size_t)tc * HG : nullptr, o);
-      float* pt = part + (size_t)task * 128;
-      pt[g4 * 8 + 2 * tg] = o[0];
-      pt[g4 * 8 + 2 * tg + 1] = o[1];
-      pt[(g4 + 8) * 8 + 2 * tg] = o[2];
-      pt[(g4 + 8) * 8 + 2 * tg + 1] = o[3];
-    }
-    __syncthreads();
-    // SwiGLU of the unit's 8 pairs for each token, k-splits summed in order;
-    // one 16-byte entry of h per token: pairs (0, 4), (1, 5), (2, 6), (3, 7)
-    if (tid < n_e) {
-      const int nt = tid >> 3, col = tid & 7;
-      float hv[8];
-      float s8 = 0.f;
+  if (lane == 0) {
+    if (nitems > 0) issue(0);
+    if (nitems > 1) issue(1);
+  }
+  float o[8][4];
+  for (int q = 0; q < nitems; ++q) {
+    const UnitInfo U = unit_info(a, unit_of(q), n_used, n_slots);
+    const int part = q % NH, s = q & 1;
+    if (part == 0) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float gsum = 0.f, usum = 0.f;
-        for (int ks = 0; ks < kspl; ++ks) {
-          const float* pt = part + (size_t)(nt * kspl + ks) * 128;
-          gsum += pt[(2 * q) * 8 + col];
-          usum += pt[(2 * q + 1) * 8 + col];
-        }
-        hv[q] = ok ? silu_f(gsum) * usum : 0.f;
-      }
-      uint32_t hb[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        hb[q] = f32_to_bf16_rne(hv[q]);
-        s8 += __uint_as_float(hb[q] << 16);
-      }
-      const size_t row = (size_t)hrow0 + tid;
-      const int i0 = 8 * tile;  // first h index of the unit
-      uint4* dst = reinterpret_cast<uint4*>(a.hperm + row * I) + (i0 >> 5) * 4 + ((i0 & 31) >> 3);
-      *dst = make_uint4(hb[0] | (hb[4] << 16), hb[1] | (hb[5] << 16), hb[2] | (hb[6] << 16),
-                        hb[3] | (hb[7] << 16));
-      a.hs8[row * (I / 8) + tile] = s8;
+      for (int nt = 0; nt < 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     }
-    __syncthreads();
-    if (tid == 0 && i + kGuRing < nu) issue(i + kGuRing);
+    wait_bar(&mbar[s], (uint32_t)(q >> 1) & 1u, a.err);
+    __syncwarp();
+    const uint32_t tile = ptx::smem_u32(slots + (size_t)s * pslot);
+    const uint32_t* sb = reinterpret_cast<const uint32_t*>(sbuf + (size_t)((q / NH) & 1) * a.gu_sb);
+    const int ntiles = (U.n_e + 7) >> 3;
+    if (ntiles <= 1)
+      gu_unit_part<NJ, LCPG, 1>(a, U, part, tile, sb, o);
+    else if (ntiles <= 2)
+      gu_unit_part<NJ, LCPG, 2>(a, U, part, tile, sb, o);
+    else if (ntiles <= 4)
+      gu_unit_part<NJ, LCPG, 4>(a, U, part, tile, sb, o);
+    else
+      gu_unit_part<NJ, LCPG, 8>(a, U, part, tile, sb, o);
+    if (part == NH - 1) {
+      if (ntiles <= 1)
+        gu_epilogue<1>(a, U, o);
+      else if (ntiles <= 2)
+        gu_epilogue<2>(a, U, o);
+      else if (ntiles <= 4)
+        gu_epilogue<4>(a, U, o);
+      else
+        gu_epilogue<8>(a, U, o);
+    }
+    __syncwarp();  // every lane is past its reads of slot s
+    if (lane == 0 && q + 2 < nitems) issue(q + 2);
   }
 }
 
-// Down + combine.  CTA c owns rows 16 c .. 16 c + 15 of y.  The used experts
-// (and the shared one, last) come in batches of kDnBatch: thread 0 keeps two
-// batches of 16-row down tiles in flight; the warps take (expert, token tile)
-// tasks and leave each pair's 16 outputs in shared memory; then every token's
-// rows are combined in the order of its top-k, the gated shared expert last.
+// Down + combine.  CTA c owns rows 16 c .. 16 c + 15 of y.  Work items: every
+// used expert (all of its token tiles at once), then the shared expert one
+// token tile per item; warp w takes items w, w + 8, ... through two slots of
+// its own and leaves each (row, pair) output in shared memory; after one
+// barrier every token's rows are combined in the order of its top-k, the
+// gated shared expert last.
+template <int LCPG, int NT>
+__device__ __forceinline__ void dn_item(const BArgs& a, int hrow0, int n_e, int nt0, bool ok,
+                                        uint32_t tile, TileGeom geo, const uint32_t* sb,
+                                        float* oc) {
+  const int IG = a.I >> (LCPG + 5), IC = a.I / 32;
+  const int lane = threadIdx.x & 31, g4 = lane >> 2, tg = lane & 3;
+  int tb[NT], ta[NT], tc[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int base = (nt0 + nt) * 8;
+    tb[nt] = (ok && base + g4 < n_e) ? hrow0 + base + g4 : -1;
+    ta[nt] = base + 2 * tg < n_e ? hrow0 + base + 2 * tg : -1;
+    tc[nt] = base + 2 * tg + 1 < n_e ? hrow0 + base + 2 * tg + 1 : -1;
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  if (ok)
+    tile_mn<LCPG, NT>(tile, geo, 0, IC, 0, a.hperm, a.I, tb, ta, tc, sb + g4 * IG,
+                      sb + (g4 + 8) * IG, a.hg, IG, o);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    if (ta[nt] >= 0) {
+      oc[(size_t)ta[nt] * 16 + g4] = o[nt][0];
+      oc[(size_t)ta[nt] * 16 + g4 + 8] = o[nt][2];
+    }
+    if (tc[nt] >= 0) {
+      oc[(size_t)tc[nt] * 16 + g4] = o[nt][1];
+      oc[(size_t)tc[nt] * 16 + g4 + 8] = o[nt][3];
+    }
+  }
+}
+
 template <int LCPG>
 __global__ void __launch_bounds__(kBThreads, 1) bdec_down_kernel(const BArgs a, int H) {
   const int I = a.I, k = a.k, T = a.T, P = a.P;
-  const int IG = I >> (LCPG + 5), IC = I / 32;
+  const int IG = I >> (LCPG + 5);
   const bool dswz = I / 2 >= 128;
   const uint32_t pitch = dswz ? 128u : (uint32_t)(I / 2);
   const int ncbd = dswz ? I / 256 : 1;
@@ -333,120 +433,77 @@ __global__ void __launch_bounds__(kBThreads, 1) bdec_down_kernel(const BArgs a, 
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
   float* oc = reinterpret_cast<float*>(sm + a.ocache);  // [P + T][16]
-  uint64_t* mbar =
-      reinterpret_cast<uint64_t*>(sm + a.ocache + (((size_t)(P + T) * 64 + 15) & ~size_t(15)));
-  __shared__ int s_first[kDnBatch + 1];  // first task of each expert of the batch
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, tg = lane & 3;
+  uint8_t* slots = sm + (size_t)warp * 2 * a.dn_slot;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(
+                       sm + a.ocache + (((size_t)(P + T) * 64 + 15) & ~size_t(15))) + warp * 2;
   const DecLayer* L = a.L;
   const int n_slots = L->n_slots;
   const int r0 = 16 * (int)blockIdx.x;
   const int n_used = *a.n_used;
-  const int nexp = n_used + 1;
-  const int nb = (nexp + kDnBatch - 1) / kDnBatch;
+  const int nitem = n_used + (T + 7) / 8;  // routed experts, then the shared expert's token tiles
+  const int nw = nitem > warp ? (nitem - warp + kBWarps - 1) / kBWarps : 0;
   const uint32_t tile_bytes = (uint32_t)ncbd * 16 * pitch;
-  if (tid == 0) {
-    for (int i = 0; i < 2 * kDnBatch; ++i) ptx::mbar_init(&mbar[i], 1);
+  if (lane == 0) {
+    ptx::mbar_init(&mbar[0], 1);
+    ptx::mbar_init(&mbar[1], 1);
     ptx::fence_mbar_init();
   }
-  __syncthreads();
-  // per expert of the list: its pairs (positions in perm) or the shared expert's tokens
-  auto expert = [&](int ue, int& pos0, int& n_e, int& hrow0, bool& ok) {
-    if (ue < n_used) {
-      const int e = a.used[ue];
-      pos0 = a.offsets[e];
-      n_e = min(a.offsets[e + 1] - pos0, kBMaxT);
-      hrow0 = pos0;
-      ok = slot_of(a, e, n_slots) >= 0;
+  __syncwarp();
+  auto issue = [&](int j) {  // lane 0: this warp's j-th item into slot j & 1
+    const int q = warp + kBWarps * j;
+    const int s = j & 1;
+    uint8_t* dst = slots + (size_t)s * a.dn_slot;
+    ptx::fence_proxy_async_smem();
+    if (q < n_used) {
+      const int slot = slot_of(a, a.used[q], n_slots);
+      if (slot < 0) {
+        record_error(a.err, MOE_ERR_SLOT);
+        ptx::mbar_arrive_expect_tx(&mbar[s], 0);
+        return;
+      }
+      ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
+      ptx::tma_load_4d(dst, &L->map_d, 0, r0, 0, slot, &mbar[s]);
+      ptx::bulk_g2s(dst + a.dn_sb,
+                    L->pool + (uint64_t)slot * L->stride + L->d_sb + (uint64_t)r0 * IG * 4,
+                    16u * IG * 4, &mbar[s]);
     } else {
-      pos0 = 0;
-      n_e = T;
-      hrow0 = P;
-      ok = true;
+      ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
+      ptx::tma_load_4d(dst, &L->map_sd, 0, r0, 0, 0, &mbar[s]);
+      ptx::bulk_g2s(dst + a.dn_sb, L->shared_blob + L->d_sb + (uint64_t)r0 * IG * 4,
+                    16u * IG * 4, &mbar[s]);
     }
   };
-  auto issue_batch = [&](int b) {  // thread 0
-    ptx::fence_proxy_async_smem();  // the slots' previous tiles were read by ldmatrix
-    for (int j = 0; j < kDnBatch; ++j) {
-      const int ue = b * kDnBatch + j;
-      if (ue >= nexp) break;
-      const int s = (b & 1) * kDnBatch + j;
-      uint8_t* dst = sm + (size_t)s * a.dn_slot;
-      if (ue < n_used) {
-        const int slot = slot_of(a, a.used[ue], n_slots);
-        if (slot < 0) {
-          record_error(a.err, MOE_ERR_SLOT);
-          ptx::mbar_arrive_expect_tx(&mbar[s], 0);
-          continue;
-        }
-        ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
-        ptx::tma_load_4d(dst, &L->map_d, 0, r0, 0, slot, &mbar[s]);
-        ptx::bulk_g2s(dst + a.dn_sb,
-                      L->pool + (uint64_t)slot * L->stride + L->d_sb + (uint64_t)r0 * IG * 4,
-                      16u * IG * 4, &mbar[s]);
-      } else {
-        ptx::mbar_arrive_expect_tx(&mbar[s], tile_bytes + 16u * IG * 4);
-        ptx::tma_load_4d(dst, &L->map_sd, 0, r0, 0, 0, &mbar[s]);
-        ptx::bulk_g2s(dst + a.dn_sb, L->shared_blob + L->d_sb + (uint64_t)r0 * IG * 4,
-                      16u * IG * 4, &mbar[s]);
-      }
-    }
-  };
-  if (tid == 0) {
-    issue_batch(0);
-    if (nb > 1) issue_batch(1);
+  if (lane == 0) {
+    if (nw > 0) issue(0);
+    if (nw > 1) issue(1);
   }
-  for (int b = 0; b < nb; ++b) {
-    if (tid == 0) {
-      int acc = 0;
-      for (int j = 0; j < kDnBatch; ++j) {
-        s_first[j] = acc;
-        const int ue = b * kDnBatch + j;
-        if (ue < nexp) {
-          int pos0, n_e, hrow0;
-          bool ok;
-          expert(ue, pos0, n_e, hrow0, ok);
-          acc += (n_e + 7) >> 3;
-        }
-      }
-      s_first[kDnBatch] = acc;
+  for (int j = 0; j < nw; ++j) {
+    const int q = warp + kBWarps * j, s = j & 1;
+    wait_bar(&mbar[s], (uint32_t)(j >> 1) & 1u, a.err);
+    __syncwarp();
+    const uint32_t tile = ptx::smem_u32(slots + (size_t)s * a.dn_slot);
+    const uint32_t* sb = reinterpret_cast<const uint32_t*>(slots + (size_t)s * a.dn_slot + a.dn_sb);
+    if (q < n_used) {
+      const int e = a.used[q];
+      const int pos0 = a.offsets[e], n_e = min(a.offsets[e + 1] - pos0, kBMaxT);
+      const bool ok = slot_of(a, e, n_slots) >= 0;
+      const int ntiles = (n_e + 7) >> 3;
+      if (ntiles <= 1)
+        dn_item<LCPG, 1>(a, pos0, n_e, 0, ok, tile, geo, sb, oc);
+      else if (ntiles <= 2)
+        dn_item<LCPG, 2>(a, pos0, n_e, 0, ok, tile, geo, sb, oc);
+      else if (ntiles <= 4)
+        dn_item<LCPG, 4>(a, pos0, n_e, 0, ok, tile, geo, sb, oc);
+      else
+        dn_item<LCPG, 8>(a, pos0, n_e, 0, ok, tile, geo, sb, oc);
+    } else {
+      dn_item<LCPG, 1>(a, P, T, q - n_used, true, tile, geo, sb, oc);
     }
-    __syncthreads();
-    const int ntask = s_first[kDnBatch];
-    for (int task = warp; task < ntask; task += kBWarps) {
-      int j = 0;
-      while (j + 1 < kDnBatch && s_first[j + 1] <= task) ++j;
-      const int nt = task - s_first[j];
-      const int ue = b * kDnBatch + j, s = (b & 1) * kDnBatch + j;
-      int pos0, n_e, hrow0;
-      bool ok;
-      expert(ue, pos0, n_e, hrow0, ok);
-      wait_bar(&mbar[s], (uint32_t)(b >> 1) & 1u, a.err);
-      const int ib = nt * 8 + g4, ia = nt * 8 + 2 * tg, ic = ia + 1;
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
-      if (ok) {
-        const uint32_t* sb =
-            reinterpret_cast<const uint32_t*>(sm + (size_t)s * a.dn_slot + a.dn_sb);
-        const uint4* b_src =
-            ib < n_e ? reinterpret_cast<const uint4*>(a.hperm + (size_t)(hrow0 + ib) * I) + tg
-                     : nullptr;
-        tile_task_n<LCPG>(ptx::smem_u32(sm + (size_t)s * a.dn_slot), geo, 0, IC, b_src,
-                          sb + g4 * IG, sb + (g4 + 8) * IG,
-                          ia < n_e ? a.hg + (size_t)(hrow0 + ia) * IG : nullptr,
-                          ic < n_e ? a.hg + (size_t)(hrow0 + ic) * IG : nullptr, o);
-      }
-      if (ia < n_e) {
-        oc[(size_t)(hrow0 + ia) * 16 + g4] = o[0];
-        oc[(size_t)(hrow0 + ia) * 16 + g4 + 8] = o[2];
-      }
-      if (ic < n_e) {
-        oc[(size_t)(hrow0 + ic) * 16 + g4] = o[1];
-        oc[(size_t)(hrow0 + ic) * 16 + g4 + 8] = o[3];
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && b + 2 < nb) issue_batch(b + 2);
+    __syncwarp();
+    if (lane == 0 && j + 2 < nw) issue(j + 2);
   }
+  __syncthreads();
   // combine: rows 2 q and 2 q + 1 of token t per thread
   for (int w = tid; w < T * 8; w += kBThreads) {
     const int t = w >> 3, q = w & 7;
@@ -602,15 +659,18 @@ bool bplan(const Dims& d, int T, BPlan& p) {
   const bool dswz = I / 2 >= 128;
   const uint64_t pitch = dswz ? 128 : (uint64_t)(I / 2);
   const uint64_t ncbd = dswz ? (uint64_t)(I / 256) : 1;
-  p.gu_sb = (uint32_t)NCB * 2048;
-  p.gu_slot = up_u32((uint64_t)p.gu_sb + 16ull * HG * 4, 1024);
-  p.part = kGuRing * p.gu_slot;
-  p.smem_gu = p.part + kBWarps * 16 * 8 * 4 + kGuRing * 8 + 1024;
+  // gate/up: per warp two part slots (16 rows x the column blocks of a part)
+  // and two scale buffers; the barriers last
+  const int NH = NCB >= 2 ? 2 : 1;
+  p.gu_slot = (uint32_t)(NCB / NH) * 2048;
+  p.gu_sb = up_u32(16ull * HG * 4, 16);
+  p.part = kBWarps * 2 * (p.gu_slot + p.gu_sb);
+  p.smem_gu = p.part + kBWarps * 2 * 8 + 1024;
   p.dn_sb = up_u32(ncbd * 16 * pitch, 128);
   p.dn_slot = up_u32((uint64_t)p.dn_sb + 16ull * IG * 4, 1024);
-  p.ocache = 2 * kDnBatch * p.dn_slot;
+  p.ocache = kBWarps * 2 * p.dn_slot;  // two slots per warp, then the outputs
   const uint64_t rows = (uint64_t)T * d.k + T;
-  p.smem_dn = (uint32_t)(p.ocache + ((rows * 64 + 15) & ~15ull) + 2 * kDnBatch * 8 + 1024);
+  p.smem_dn = (uint32_t)(p.ocache + ((rows * 64 + 15) & ~15ull) + kBWarps * 2 * 8 + 1024);
   return T >= 2 && T <= kBMaxT && decode_shape_ok(d) && p.smem_gu <= kBSmemMax &&
          p.smem_dn <= kBSmemMax;
 }

@@ -1187,7 +1187,7 @@ size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 // slot_stride}; box {128, box_rows, all column blocks, 1}, the 128-byte
 // swizzle.  Rows shorter than 128 bytes are one unswizzled column block.
 bool encode_rows(CUtensorMap* m, const uint8_t* base, int row_bytes, int rows, int slots,
-                 uint64_t slot_stride, int box_rows) {
+                 uint64_t slot_stride, int box_rows, int box_cbs = 0) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const bool swz = row_bytes >= 128;
@@ -1198,7 +1198,9 @@ bool encode_rows(CUtensorMap* m, const uint8_t* base, int row_bytes, int rows, i
       slots > 1 ? (cuuint64_t)slot_stride : ((cuuint64_t)rows * row_bytes + 15) / 16 * 16;
   const cuuint64_t dim[4] = {inner, (cuuint64_t)rows, ncb, (cuuint64_t)slots};
   const cuuint64_t stride[3] = {(cuuint64_t)row_bytes, inner, sstride};
-  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)box_rows, (cuuint32_t)ncb, 1};
+  // box_cbs > 0: that many column blocks per box (a part of each row)
+  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)box_rows,
+                             (cuuint32_t)(box_cbs > 0 ? box_cbs : ncb), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dim, stride, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1230,7 +1232,12 @@ bool decode_encode_maps(const Dims& d, const uint8_t* pool, const BlobLayout& ex
   return encode_rows(&D->map_gu, pool + ex.gu_q, d.H / 2, 2 * d.I, n_slots, ex.stride, 8) &&
          encode_rows(&D->map_d, pool + ex.d_q, d.I / 2, d.H, n_slots, ex.stride, 16) &&
          encode_rows(&D->map_sgu, shared + sh.gu_q, d.H / 2, 2 * d.Is, 1, sh.stride, 8) &&
-         encode_rows(&D->map_sd, shared + sh.d_q, d.Is / 2, d.H, 1, sh.stride, 16);
+         encode_rows(&D->map_sd, shared + sh.d_q, d.Is / 2, d.H, 1, sh.stride, 16) &&
+         // half rows (batched decode): 8-row boxes of half the column blocks
+         encode_rows(&D->map_guh, pool + ex.gu_q, d.H / 2, 2 * d.I, n_slots, ex.stride, 8,
+                     std::max(1, d.H / 512)) &&
+         encode_rows(&D->map_sguh, shared + sh.gu_q, d.H / 2, 2 * d.Is, 1, sh.stride, 8,
+                     std::max(1, d.H / 512));
 }
 
 cudaError_t decode_prepare(const Dims& d, int nC, bool chain, int* ok) {

@@ -58,6 +58,8 @@ struct alignas(64) DecLayer {
   // routed gate/up 2I rows of H/2 bytes, box 8 rows; routed down H rows of
   // I/2 bytes, box 16 rows; the shared expert's the same with one slot
   CUtensorMap map_gu, map_d, map_sgu, map_sd;
+  // the same gate/up maps with boxes of half the column blocks (batched decode)
+  CUtensorMap map_guh, map_sguh;
   const uint16_t* router_w;       // [E][H]
   const float* prior;             // [E] or null
   const uint16_t* shared_gate_w;  // [H]

@@ -53,6 +53,7 @@ def test_batched_decode_deterministic_and_equals_single_tokens():
     W = synth.layer_weights(0, wl.wid, 82, wl.shape)
     T = 6
     L = U.layer(wl.shape, W, max_T=T)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
     x = synth.tokens(0, wl.wid, 82, 0, T, wl.H)
     a, b = U.run(L, x), U.run(L, x)
     assert np.array_equal(a["y_bits"], b["y_bits"])
