@@ -182,3 +182,42 @@ def tokens(seed: int, workload: int, layer: int, step: int, T: int, H: int) -> n
     x = np.empty((T, H), np.uint16)
     _load().synth_fill_tokens(seed, workload, layer, step, T, H, _ptr(x))
     return x
+
+
+# Tensor ids of the Gated DeltaNet recurrence inputs.
+T_GDN_Q, T_GDN_K, T_GDN_V, T_GDN_ALPHA, T_GDN_BETA, T_GDN_STATE = 31, 32, 33, 34, 35, 36
+
+
+def uniform_f32(key: int, n: int, lo: float, hi: float) -> np.ndarray:
+    """n float32 values uniform in [lo, hi): the top 24 bits of each draw."""
+    u = (uniform_u32(key, n) >> np.uint32(8)).astype(np.float64) * (1.0 / (1 << 24))
+    return (lo + (hi - lo) * u).astype(np.float32)
+
+
+@dataclass(frozen=True)
+class GdnShape:
+    """Sizes of one Gated DeltaNet layer's recurrence: Hk key heads, Hv value
+    heads (a multiple of Hk), key dim dk, value dim dv."""
+    Hk: int = 16
+    Hv: int = 32
+    dk: int = 128
+    dv: int = 128
+
+
+def gdn_inputs(seed: int, layer: int, B: int, T: int, s: GdnShape, step: int = 0,
+               alpha_lo: float = 0.80, state_std: float = 0.5):
+    """Inputs of B independent sequences, T tokens each:
+    q, k bf16 [B,T,Hk,dk] ~ N(0,1); v bf16 [B,T,Hv,dv] ~ N(0,1);
+    alpha f32 [B,T,Hv] uniform in [alpha_lo, 1); beta f32 [B,T,Hv] uniform in [0, 1);
+    state f32 [B,Hv,dv,dk] ~ N(0, state_std^2) (bf16 values widened)."""
+    def key(t):
+        return stream_key(seed, 9, layer, t, step)
+    nq = B * T * s.Hk * s.dk
+    q = normal_bf16(key(T_GDN_Q), nq).reshape(B, T, s.Hk, s.dk)
+    k = normal_bf16(key(T_GDN_K), nq).reshape(B, T, s.Hk, s.dk)
+    v = normal_bf16(key(T_GDN_V), B * T * s.Hv * s.dv).reshape(B, T, s.Hv, s.dv)
+    alpha = uniform_f32(key(T_GDN_ALPHA), B * T * s.Hv, alpha_lo, 1.0).reshape(B, T, s.Hv)
+    beta = uniform_f32(key(T_GDN_BETA), B * T * s.Hv, 0.0, 1.0).reshape(B, T, s.Hv)
+    sb = normal_bf16(key(T_GDN_STATE), B * s.Hv * s.dv * s.dk, 0.0, state_std)
+    state = (sb.astype(np.uint32) << 16).view(np.float32).reshape(B, s.Hv, s.dv, s.dk)
+    return q, k, v, alpha, beta, state
