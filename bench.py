@@ -53,10 +53,16 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--path", type=int, default=0, help="kernel path (0 auto)")
-    p.add_argument("--mode", choices=["auto", "stack", "layers"], default="auto",
+    p.add_argument("--mode", choices=["auto", "stack", "layers", "gdn"], default="auto",
                    help="one-token workloads: 'stack' chains the layers (RMSNorm + residual) "
                         "in one persistent launch per token; 'layers' runs independent "
                         "layers, one moe_forward each (auto: stack)")
+    p.add_argument("--gdn-batch", type=int, default=64,
+                   help="--mode gdn: independent sequences per launch")
+    p.add_argument("--gdn-tokens", type=int, default=1,
+                   help="--mode gdn: tokens per sequence per launch (1 = decode)")
+    p.add_argument("--gdn-layers", type=int, default=36,
+                   help="--mode gdn: Gated DeltaNet layers per step (own state each)")
     p.add_argument("--pool-slots", type=int, default=0,
                    help="bounded slot pool of this many resident experts per layer (the rest "
                         "in pinned host memory, LFU + recency eviction); implies --mode layers")
@@ -109,10 +115,11 @@ def peaks():
 # (profiles/traffic.json), with the hash of the sources they were taken on:
 # reported only while those sources are unchanged.
 TRAFFIC_SOURCES = {
-    "decode_kernel": ["decode.cu", "routing_common.cuh", "device_util.cuh", "sm100_ptx.cuh",
-                      "moe_internal.cuh"],
+    "decode_kernel": ["decode.cu", "gemv_mma.cuh", "routing_common.cuh", "device_util.cuh",
+                      "sm100_ptx.cuh", "moe_internal.cuh"],
     "fused_decode_kernel": ["fused_decode.cu", "routing_common.cuh", "device_util.cuh",
                             "sm100_ptx.cuh", "moe_internal.cuh"],
+    "gdn_recurrence_kernel": ["gdn.cu", "sm100_ptx.cuh"],
     "grouped_gemm_kernel<gate/up>": ["prefill.cu", "device_util.cuh", "sm100_ptx.cuh",
                                      "moe_internal.cuh"],
 }
@@ -732,6 +739,173 @@ def run_ours_stack(args, wl):
         torch.distributed.destroy_process_group()
 
 
+GDN_SHAPE = synth.GdnShape(Hk=16, Hv=32, dk=128, dv=128)
+
+
+def gdn_oracle_rate(budget_s, Lg):
+    """The float64 oracle on whole sequence-layers of the decode workload
+    (one token each) for about budget_s seconds: sequence-layers/s."""
+    from oracle import gdn_oracle as G
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        q, k, v, a, b, S0 = synth.gdn_inputs(0, done % Lg, 1, 1, GDN_SHAPE, step=done)
+        G.gdn_recurrence(q, k, v, a, b, S0)
+        done += 1
+    return done / (time.perf_counter() - t0), done
+
+
+def run_gdn(args):
+    """Gated DeltaNet decode: every step runs `gdn_layers` launches, one per
+    layer, each advancing B sequences by T tokens with its own state."""
+    import torch
+
+    import int4_routed_expert_decode_gb300 as moe
+    from int4_routed_expert_decode_gb300 import build as moe_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    moe_build.build()
+    s, B, T, Lg = GDN_SHAPE, args.gdn_batch, args.gdn_tokens, args.gdn_layers
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if a.dtype == np.uint16
+                                                            else a.dtype)).cuda()
+
+    # Per layer its own state buffer (layers past the first few start from a
+    # device copy of an earlier layer's seeded state); the token inputs of a
+    # few distinct seeded draws rotate over layers and steps.
+    S = max(1, min(args.distinct, 4, Lg))
+    states, ins = [], []
+    for l in range(S):
+        q, k, v, a, b, S0 = synth.gdn_inputs(0, l, B, T, s)
+        states.append(dev(S0))
+        ins.append(tuple(dev(x) for x in (q, k, v, a, b)))
+    for l in range(S, Lg):
+        states.append(states[l % S].clone())
+    out = torch.empty((B, T, s.Hv, s.dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def enqueue(step, inputs=None):
+        for l in range(Lg):
+            q, k, v, a, b = inputs or ins[(step + l) % len(ins)]
+            moe.moe_gdn_recurrence(q, k, v, a, b, states[l], out, B, T, s.Hk, s.Hv, s.dk, s.dv,
+                                   stream=stream.cuda_stream)
+
+    # parity spot check of sequence 0 and B-1 of layer 0, first step, against the oracle
+    parity = None
+    if rank == 0 and not args.profile:
+        from oracle import gdn_oracle as G
+        q, k, v, a, b, S0 = synth.gdn_inputs(0, 0, B, T, s)
+        with torch.cuda.stream(stream):
+            st0 = states[0].clone()
+            o0 = torch.empty_like(out)
+            qd, kd, vd, ad, bd = ins[0]
+            moe.moe_gdn_recurrence(qd, kd, vd, ad, bd, st0, o0, B, T, s.Hk, s.Hv, s.dk, s.dv,
+                                   stream=stream.cuda_stream)
+            stream.synchronize()
+        errs = []
+        for i in sorted({0, B - 1}):
+            ro, rS = G.gdn_recurrence(q[i:i + 1], k[i:i + 1], v[i:i + 1], a[i:i + 1], b[i:i + 1],
+                                      S0[i:i + 1])
+            scale = max(1.0, float(np.abs(rS).max()))
+            errs.append(max(float(np.abs(o0[i].cpu().numpy() - ro[0]).max()),
+                            float(np.abs(st0[i].cpu().numpy() - rS[0]).max())) / scale)
+        parity = {"checked_sequences": sorted({0, B - 1}), "max_rel_err": max(errs)}
+
+    clocks = ClockSampler(local).start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            enqueue(i)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            enqueue(args.warmup + i)
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    t_max = max_over_ranks(ms, world, "cuda")
+    ms_step = t_max / args.steps
+    units = world * B * Lg * args.steps  # sequence-layers advanced by T tokens
+    value = units / (t_max / 1e3)
+    us_launch = ms_step * 1e3 / Lg
+    state_bytes = B * s.Hv * s.dv * s.dk * 4
+    in_bytes = B * T * (2 * s.Hk * s.dk * 2 + s.Hv * s.dv * 2 + 2 * s.Hv * 4)
+    out_bytes = B * T * s.Hv * s.dv * 4
+    algo = 2 * state_bytes + in_bytes + out_bytes
+    pk = peaks()
+    achieved = algo / (us_launch * 1e-6) / 1e9
+
+    # e2e: host inputs in and the outputs back, every launch, pinned buffers
+    hin = [x.cpu().pin_memory() for x in ins[0]]
+    din = [torch.empty_like(x) for x in ins[0]]
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    k_e2e = 1 if args.profile else max(1, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            for l in range(Lg):
+                for d, h in zip(din, hin):
+                    d.copy_(h, non_blocking=True)
+                q, k, v, a, b = din
+                moe.moe_gdn_recurrence(q, k, v, a, b, states[l], out, B, T, s.Hk, s.Hv, s.dk,
+                                       s.dv, stream=stream.cuda_stream)
+                hout.copy_(out, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / k_e2e
+    e2e = {"value": world * B * Lg / (ms_e2e / 1e3), "unit": "sequence-layers/s",
+           "h2d_bytes_per_step": Lg * in_bytes, "d2h_bytes_per_step": Lg * out_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
+        rate, n = gdn_oracle_rate(min(args.cpu_budget, 10.0), Lg)
+        cpu = {"value": rate, "unit": "sequence-layers/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} sequence-layers (one token, 32 heads of 128x128 state each), "
+                         "float64 numpy oracle"}
+    line = {
+        "metric": "gdn_decode_sequence_layers_per_s", "value": value,
+        "unit": "sequence-layers/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": {"workload": f"gdn_decode: {Lg} Gated DeltaNet layers x {B} sequences, "
+                               f"{T} token(s) each", "Hk": s.Hk, "Hv": s.Hv, "dk": s.dk,
+                   "dv": s.dv, "sequences": B, "tokens": T, "layers": Lg,
+                   "parallelism": "replicas",
+                   "l2": f"inputs larger than L2: {Lg * state_bytes / 1e9:.2f} GB of state "
+                         "streamed per step"},
+        "us_per_launch": us_launch,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": measured_traffic(
+                         "gdn_recurrence_kernel", f"gdn_B{B}_T{T}"),
+                     "kernel": f"gdn_recurrence_kernel, {algo / 1e6:.1f} MB algorithmic per "
+                               f"launch ({us_launch:.2f} us per launch)",
+                     "peak_source": pk["source"]},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": args.steps * Lg,
+        "parity_spot_check": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 PHASES = [(0, "start"), (1, "input"), (25, "router_dots"), (2, "router"), (8, "logits_in"),
           (7, "sel_minmax"), (13, "sel_scan"), (14, "sel_cand"), (21, "rank"), (22, "certified"),
           (23, "slots"), (3, "select"), (24, "gu_first_task"), (9, "gu_tasks"), (4, "gateup"),
@@ -803,7 +977,9 @@ def main():
     if args.phases:
         run_phases(args, wl)
         return
-    if args.impl == "reference":
+    if args.mode == "gdn":
+        run_gdn(args)
+    elif args.impl == "reference":
         run_reference(args, wl)
     elif stack_mode(args, wl):
         run_ours_stack(args, wl)

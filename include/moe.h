@@ -378,6 +378,38 @@ int moe_stack_set_test_flags(moe_stack* s, int flags);
 /* Free the stack's device memory (synchronises the device).  NULL is a no-op. */
 void moe_stack_destroy(moe_stack* s);
 
+/* ---- Gated DeltaNet recurrence --------------------------------------------
+ * The linear-attention layers of the same hybrid stack (three quarters of its
+ * layers: wpnews page, Swiftlet README, "How it works"; creativeainews page,
+ * "How Expert Streaming Works") carry a fixed-size state per value head
+ * instead of a KV cache.  The pages print no equations; this call computes
+ * the plain gated delta rule, for each value head h and token t:
+ *   k^ = k / sqrt(|k|^2 + 1e-6),  q^ = q / sqrt(|q|^2 + 1e-6) / sqrt(dk)
+ *   S  = alpha S + beta (v - alpha S k^) k^T,   o = S q^   (S after the update)
+ * where value head h reads key head h / (Hv / Hk).  The gates alpha and beta,
+ * the short convolution before it and the norm and projection after it belong
+ * to the rest of the layer: alpha and beta arrive computed.
+ *   q, k    bf16 [B][T][Hk][dk] device, aligned to dk/16 bytes
+ *   v       bf16 [B][T][Hv][dv] device
+ *   alpha   fp32 [B][T][Hv] device (decay, normally in [0, 1])
+ *   beta    fp32 [B][T][Hv] device (write strength, normally in [0, 1])
+ *   state   fp32 [B][Hv][dv][dk] device, 16-byte aligned, row i of a head's
+ *           state holds its dk columns contiguously; read, then overwritten
+ *           with the state after token T-1 (in place)
+ *   out     fp32 [B][T][Hv][dv] device, written; must not overlap the inputs
+ * B independent sequences of T tokens each (T = 1 is a decode step; T > 1
+ * runs the tokens in order, the state kept in registers in between).
+ * Sizes: dk in {64, 128, 256} (else MOE_ERR_UNSUPPORTED); B, T >= 0 (either 0:
+ * nothing happens); Hk >= 1; Hv a multiple of Hk; dv in [1, 4096];
+ * B*Hv*dv <= 2^33.  Other sizes, a NULL or misaligned pointer return
+ * MOE_ERR_INVALID_ARG with a message for moe_last_error(NULL) and launch
+ * nothing; a launch failure returns MOE_ERR_CUDA.  No context, no allocation;
+ * asynchronous on `stream`; calls on different streams over disjoint states
+ * may overlap. */
+int moe_gdn_recurrence(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const float* alpha, const float* beta, float* state, float* out,
+                       int B, int T, int Hk, int Hv, int dk, int dv, void* stream);
+
 /* The last message of `ctx` (NULL: of the calls without a context), and the
  * name of a status code.  Never NULL. */
 const char* moe_last_error(const moe_ctx* ctx);

@@ -39,6 +39,7 @@ EXPORTS = (
     "moe_route_static", "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
     "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags", "moe_stack_destroy",
     "moe_router_check_stats", "moe_pool_enable", "moe_pool_stats", "moe_pool_table",
+    "moe_gdn_recurrence",
 )
 
 
@@ -113,6 +114,8 @@ def lib():
     L.moe_pool_table.argtypes = [vp, vp]
     L.moe_pool_table.restype = i32
     L.moe_stack_destroy.argtypes = [vp]
+    L.moe_gdn_recurrence.argtypes = [vp] * 7 + [i32] * 6 + [vp]
+    L.moe_gdn_recurrence.restype = i32
     L.moe_stack_destroy.restype = None
     for name in ("moe_create", "moe_load_weights", "moe_reserve", "moe_forward", "moe_get_status",
                  "moe_read_expert", "moe_set_path", "moe_last_launch_count",
@@ -278,6 +281,15 @@ def moe_route_static(x, T: int, router_w, router_bias, shared_gate_w, E: int, k:
     _check(lib().moe_route_static(_addr(x), T, _addr(router_w), _addr(router_bias),
                                   _addr(shared_gate_w), E, k, hidden, _addr(topk_idx),
                                   _addr(topk_w), _addr(shared_gate), _stream(stream)))
+
+
+def moe_gdn_recurrence(q, k, v, alpha, beta, state, out, B: int, T: int, Hk: int, Hv: int,
+                       dk: int, dv: int, stream=None):
+    """Gated DeltaNet recurrence over B sequences of T tokens, state updated in
+    place (device pointers or tensors); see include/moe.h."""
+    _check(lib().moe_gdn_recurrence(_addr(q), _addr(k), _addr(v), _addr(alpha), _addr(beta),
+                                    _addr(state), _addr(out), B, T, Hk, Hv, dk, dv,
+                                    _stream(stream)))
 
 
 def moe_pool_enable(ctx: int, slots: int):

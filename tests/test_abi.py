@@ -98,3 +98,20 @@ def test_pool_calls_reject_null_arguments(L):
     assert L.moe_pool_stats(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_pool_table(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_router_check_stats(None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_gdn_recurrence_checks_arguments_before_any_launch(L):
+    """Sizes and pointers are checked on the host (no GPU needed): empty calls
+    succeed without touching anything; bad sizes are refused."""
+    import int4_routed_expert_decode_gb300 as moe
+    assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
+                                0, 1, 2, 4, 128, 8, None) == moe.MOE_OK
+    assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
+                                1, 0, 2, 4, 128, 8, None) == moe.MOE_OK
+    assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
+                                1, 1, 3, 4, 128, 8, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
+                                1, 1, 2, 4, 96, 8, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
+                                1, 1, 2, 4, 128, 8, None) == moe.MOE_ERR_INVALID_ARG
+    assert b"NULL" in L.moe_last_error(None)
