@@ -7,9 +7,8 @@
  * iPhone", wpnews), section "How it works": each layer routes every token to
  * k of E experts (8 of 256 for Qwen3.6-35B-A3B, 10 of 512 for
  * Qwen3-Next-80B-A3B), keeps a shared expert resident, and stores the experts
- * in MLX affine int4 group quantisation (same README, list of what was built:
- * "MLX affine int4/int8 group quantization", "byte-addressed kernels with
- * 64-bit offsets for multi-gigabyte shards").  For every token t:
+ * in MLX's affine int4 group quantisation, addressed with 64-bit byte
+ * offsets (same README, its list of what was built).  For every token t:
  *
  *   l[t,e]  = x_t . Wr_e (+ prior_e)                        router
  *   idx, w  = top-k of softmax(l[t,:]) (descending, ties -> lowest e),
@@ -99,9 +98,9 @@ typedef struct moe_weights {
  * no device is current. */
 int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out);
 
-/* Copy and repack the weights into library-owned device memory (the pages'
- * routed experts live in a container "built from fixed-stride blobs for fast
- * seeking", README "How it works"; MLX affine int4 layout per the list of
+/* Copy and repack the weights into library-owned device memory (on the pages
+ * the routed experts sit in a container of equal-stride records, one per
+ * expert, README "How it works"; MLX affine int4 layout per its list of
  * what was built): the routed experts become n_slots fixed-stride blobs (slot s holds the s-th expert of
  * `w`, 64-bit byte offsets), the router, prior, shared gate vector and shared
  * expert stay resident beside them.  Synchronous: when it returns the caller
@@ -121,7 +120,7 @@ int moe_reserve(moe_ctx* ctx, int max_T);
  * no host synchronisation, no allocation: capturable in a CUDA graph): the
  * router, top-k, shared expert and routed experts of README "How it works",
  * with the slot table standing for the pages' bounded expert pool.
- *   x                  bf16 [T][H] device, read only
+ *   x                  bf16 [T][H] device, 16-byte aligned, read only
  *   expert_slot_table  int32 [E] device: slot holding expert e, or NULL for
  *                      the identity (requires n_slots >= E).  A selected
  *                      expert whose slot is negative or >= n_slots makes the
@@ -234,9 +233,10 @@ int64_t moe_device_bytes(const moe_ctx* ctx);
 int moe_last_launch_count(const moe_ctx* ctx);
 
 /* ---------------------------------------------------------------- slot pool
- * The pages keep the routed experts in storage and cache the hot ones "in a
- * bounded pool with LFU plus recency eviction" (README "How it works";
- * creativeainews, "How Expert Streaming Works").  moe_pool_enable moves the
+ * The pages keep the routed experts in storage and cache the frequently used
+ * ones in a pool of bounded size whose eviction combines use frequency with
+ * recency (README "How it works"; creativeainews, "How Expert Streaming
+ * Works").  moe_pool_enable moves the
  * loaded experts (n_slots >= E, slot e = expert e) into pinned, device-mapped
  * host memory -- the store, read by the GPU over NVLink-C2C -- and keeps
  * `slots` of them (1 <= slots < E, at most 65534) in the device pool, empty

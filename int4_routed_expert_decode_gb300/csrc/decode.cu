@@ -36,8 +36,8 @@
 //   sum_c (s q_c + b) x_c = s sum_c (128 + q_c) x_c + (b - 128 s) sum_c x_c.
 // The down projection's input h (fp32) is split into bf16 hi + lo parts that
 // ride in two columns of N, so h enters with 16 significant bits.  Weights
-// are MLX affine int4 groups (Swiftlet README, wpnews page, list of what was
-// built: "MLX affine int4/int8 group quantization"); the routed/shared split
+// are MLX affine int4 groups (Swiftlet README, wpnews page, its list of what
+// was built); the routed/shared split
 // and the top-k routing follow the same README, section "How it works".
 #include <algorithm>
 

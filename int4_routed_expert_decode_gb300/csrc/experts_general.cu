@@ -7,8 +7,8 @@
 //   gate/up:  h[q, i] = silu(Wg_i . x_t) * (Wu_i . x_t)         (q = pair position)
 //   down:     o[q, r] = Wd_r . h[q, :]
 //   combine:  y[t, r] = sum_j w[t, j] o[inv[t*k + j], r] + g_t o[P + t, r]
-// with W = s*q + b per group (MLX affine int4, Swiftlet README "MLX affine
-// int4/int8 group quantization").  The affine terms are folded per 32-code
+// with W = s*q + b per group (MLX affine int4; Swiftlet README, its list of
+// what was built).  The affine terms are folded per 32-code
 // chunk: sum_c (s q_c + b) x_c = s * sum_c q_c x_c + b * sum_c x_c, the last
 // sum staged once per token.
 #include "device_util.cuh"

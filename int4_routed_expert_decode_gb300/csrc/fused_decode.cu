@@ -26,8 +26,8 @@
 //   sum_c (s q_c + b) x_c = (128 s) * sum_c (1 + q_c/128) x_c + (b - 128 s) * sum_c x_c,
 // two codes per packed fp32 FMA (FFMA2).  Each lane keeps the inputs of its
 // own chunks (x, or h in P4) in registers, read once from global memory.
-// Weights follow the MLX affine int4 group layout (Swiftlet README, "MLX
-// affine int4/int8 group quantization").
+// Weights follow the MLX affine int4 group layout (Swiftlet README, its list
+// of what was built).
 #include "device_util.cuh"
 #include "moe_internal.cuh"
 #include "routing_common.cuh"

@@ -1,8 +1,8 @@
 // pool.cu -- a bounded pool of resident expert slots, filled on the stream.
 //
-// The pages stream routed experts from storage into "a bounded pool with LFU
-// plus recency eviction" (Swiftlet README on the wpnews page, "How it
-// works"; creativeainews, "How Expert Streaming Works").  Here every expert's
+// The pages stream routed experts from storage into a pool of bounded size
+// that evicts by use frequency and recency (Swiftlet README on the wpnews
+// page, "How it works"; creativeainews, "How Expert Streaming Works").  Here every expert's
 // blob lives in pinned, device-mapped host memory (reached over NVLink-C2C)
 // and the device holds S < E slots.  After the routing of each forward call
 // and before any expert runs:

@@ -22,8 +22,8 @@
 // layout the tensor core reads from shared memory.  The packed int4 codes
 // arrive by 3-D TMA tile copies, the scale/bias words of up to 32 groups per
 // row at a time into a double-buffered window, and the weights (A) are
-// dequantised (MLX affine, w = s q + b; Swiftlet README,
-// "MLX affine int4/int8 group quantization") to bf16 straight into tensor
+// dequantised (MLX affine, w = s q + b; Swiftlet README, its list of what
+// was built) to bf16 straight into tensor
 // memory, which the MMA reads as its A operand: A costs no shared-memory
 // bandwidth and no proxy fence.
 //

@@ -1,8 +1,8 @@
 // repack.cu -- canonical MLX affine int4 tensors <-> fixed-stride expert blobs.
 //
 // The Swiftlet README (wpnews page, "How it works") repacks the routed
-// experts "into fixed-stride blobs" so that one expert is one contiguous
-// record addressed by a 64-bit offset.  Here a blob holds, for one expert:
+// experts into records of one fixed stride, so that one expert is one
+// contiguous record addressed by a 64-bit offset.  Here a blob holds, for one expert:
 //   gu_q  [I][2][H/8]  gate row i and up row i side by side (one SwiGLU
 //                      output needs both, so a warp streams them together)
 //   gu_sb [I][2][H/G]  scale | bias << 16 per group, same row order

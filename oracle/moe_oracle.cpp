@@ -6,9 +6,8 @@
 // What it computes follows the Swiftlet project README ("Show HN: Run an 80B
 // Qwen in 4.3 GB of RAM on a Mac and a 35B on an iPhone", wpnews), section
 // "How it works": each token is routed to k of E experts, a shared expert is
-// always applied, and the experts are stored in MLX affine int4 group
-// quantisation ("MLX affine int4/int8 group quantization", same README, list
-// of what was built).  Per token t:
+// always applied, and the experts are stored in MLX's affine int4 group
+// quantisation (same README, its list of what was built).  Per token t:
 //   1. l[e] = x_t . Wr_e (+ prior_e)
 //   2. top-k of softmax(l) by the EXACT value of l (descending, ties to the
 //      lowest expert id), the k probabilities renormalised to sum to one

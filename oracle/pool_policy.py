@@ -1,11 +1,10 @@
 """Oracle of the bounded expert slot pool -- TEST INFRASTRUCTURE ONLY.
 
-The pages keep the routed experts in storage and cache "hot experts in a
-bounded pool with LFU plus recency eviction" (Swiftlet README on the wpnews
-page, section "How it works"; the same README's list of what it borrowed:
-"into a bounded slot pool ..., evict with LFU plus recency"; creativeainews,
-"How Expert Streaming Works": "evicting cold ones with a
-least-frequently-used-plus-recency policy").  They give no formula.
+The pages keep the routed experts in storage and cache the frequently used
+ones in a pool of bounded size, evicting by least frequent use combined with
+recency (Swiftlet README on the wpnews page, section "How it works", and the
+same README's list of what it borrowed; creativeainews, "How Expert Streaming
+Works").  They give no formula.
 Readings, plainest first:
 
 * one step is one forward call; the experts it needs are the distinct
