@@ -57,6 +57,8 @@ def parse():
                    help="one-token workloads: 'stack' chains the layers (RMSNorm + residual) "
                         "in one persistent launch per token; 'layers' runs independent "
                         "layers, one moe_forward each (auto: stack)")
+    p.add_argument("--bits", type=int, choices=[4, 8], default=4,
+                   help="expert code width (8: int8 experts, the general path, --mode layers)")
     p.add_argument("--gdn-batch", type=int, default=64,
                    help="--mode gdn: independent sequences per launch")
     p.add_argument("--gdn-tokens", type=int, default=1,
@@ -301,7 +303,7 @@ def run_reference(args, wl):
 
 
 def stack_mode(args, wl):
-    return wl.T == 1 and args.mode in ("auto", "stack") and not args.pool_slots
+    return wl.T == 1 and args.mode in ("auto", "stack") and not args.pool_slots and args.bits == 4
 
 
 STACK_EPS = 1e-6
@@ -312,14 +314,15 @@ def stack_norm_weights(wl, L):
     return [synth.norm_weights(0, wl.wid, l, wl.H) for l in range(L)]
 
 
-def config_of(wl, L, stacked):
+def config_of(wl, L, stacked, bits=4):
     """The workload's description; both arms print the same dict."""
-    return {"workload": wl.name, "E": wl.E, "k": wl.k, "hidden": wl.H, "inter": wl.I,
+    return {"workload": wl.name + ("-int8" if bits == 8 else ""), "E": wl.E, "k": wl.k,
+            "hidden": wl.H, "inter": wl.I,
             "shared_inter": wl.Is, "group": wl.G, "tokens_per_step": wl.T, "layers": L,
             "zipf_s": wl.zipf_s,
             "chaining": "layer l+1 consumes RMSNorm(x_l + y_l) (residual stack)" if stacked
                         else "independent layers, each with its own seeded input",
-            "weights": "int4 affine (bf16 scale+bias per group), seeded synthetic",
+            "weights": f"int{bits} affine (bf16 scale+bias per group), seeded synthetic",
             "parallelism": "replicas",
             "l2": "inputs larger than L2: every step streams distinct expert weights "
                   "far beyond the 129 MB L2; distinct step inputs rotate"}
@@ -373,9 +376,11 @@ def run_ours(args, wl):
     T, H = wl.T, wl.H
     S = max(1, min(args.distinct, args.steps + args.warmup))
     layers = []
+    weights_of = synth.layer_weights_int8 if args.bits == 8 else synth.layer_weights
     for l in range(L):
-        W = synth.layer_weights(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s)
-        layer = moe.MoELayer(wl.E, wl.k, H, wl.I, wl.Is, wl.G, weights=W, max_T=T)
+        W = weights_of(0, wl.wid, l, wl.shape, zipf_s=wl.zipf_s)
+        layer = moe.MoELayer(wl.E, wl.k, H, wl.I, wl.Is, wl.G, weights=W, max_T=T,
+                             bits=args.bits)
         if args.path:
             moe.moe_set_path(layer.ctx, args.path)
         if args.pool_slots:
@@ -399,6 +404,9 @@ def run_ours(args, wl):
                             stream=stream.cuda_stream)
 
     # eager pass per distinct input: statuses, unique experts, launch count
+    # (int8 codes take twice the int4 code bytes)
+    e_bytes = wl.expert_bytes + (3 * wl.I * wl.H // 2 if args.bits == 8 else 0)
+    s_bytes = wl.shared_bytes + (3 * wl.Is * wl.H // 2 if args.bits == 8 else 0)
     uniq_bytes = []
     ys0 = None
     with torch.cuda.stream(stream):
@@ -408,8 +416,8 @@ def run_ours(args, wl):
             if s == 0:
                 ys0 = y.clone()
             ids = idx.cpu().numpy()
-            uniq_bytes.append(sum(len(set(ids[l].ravel().tolist())) * wl.expert_bytes +
-                                  wl.shared_bytes for l in range(L)))
+            uniq_bytes.append(sum(len(set(ids[l].ravel().tolist())) * e_bytes + s_bytes
+                                  for l in range(L)))
     for l in range(L):
         st = layers[l].status(stream.cuda_stream)
         if st != moe.MOE_OK:
@@ -505,9 +513,18 @@ def run_ours(args, wl):
     cpu = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
-        cpu = cpu_baseline(wl, args.cpu_budget, L, False)
         from oracle import moe_oracle as O
-        W0 = synth.layer_weights(0, wl.wid, 0, wl.shape, zipf_s=wl.zipf_s)
+        W0 = weights_of(0, wl.wid, 0, wl.shape, zipf_s=wl.zipf_s)
+        if args.bits == 4:
+            cpu = cpu_baseline(wl, args.cpu_budget, L, False)
+        else:  # the int8 block's oracle is the numpy one, one core
+            n, t0 = 0, time.perf_counter()
+            while time.perf_counter() - t0 < min(args.cpu_budget, 10.0):
+                O.moe_block(synth.tokens(0, wl.wid, 0, n, 1, H), W0, wl.k, wl.G)
+                n += 1
+            cpu = {"value": n / (time.perf_counter() - t0), "unit": UNIT, "cores": 1,
+                   "kind": "oracle", "sample": f"{n} layer-tokens of layer 0 through the numpy "
+                                               "float64 oracle (int8 experts)"}
         rows = list(range(min(T, 4)))
         r = O.moe_block(synth.tokens(0, wl.wid, 0, 0, T, H), W0, wl.k, wl.G, tokens=rows)
         yg = ys0[0, rows].float().cpu().numpy().astype(np.float64)
@@ -518,7 +535,7 @@ def run_ours(args, wl):
     flops = {"gateup": 2.0 * H * (2 * wl.I * P + 2 * wl.Is * T),
              "down": 2.0 * H * (wl.I * P + wl.Is * T), "router": 2.0 * H * wl.E * T}
     flops_layer = sum(flops.values())
-    grouped = args.path == 3 or (args.path == 0 and T > 1)  # tensor-core grouped GEMMs
+    grouped = args.bits == 4 and (args.path == 3 or (args.path == 0 and T > 1))  # tcgen05 GEMMs
     # up to 64 tokens a layer streams each selected expert once for few tokens: HBM bound;
     # thousands of tokens make the grouped GEMMs tensor-core bound
     if grouped and T > 64 and "gateup" in stages:
@@ -546,7 +563,7 @@ def run_ours(args, wl):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if grouped else "fp32", "data": "synthetic",
-        "config": config_of(wl, L, False),
+        "config": config_of(wl, L, False, args.bits),
         "note": f"each step touches {unique_per_step / 1e6:.0f} MB of distinct expert weights; "
                 f"{S} distinct step inputs rotate",
         "us_per_layer": us_layer, "stack_tokens_per_s": world * T / (ms_step / 1e3),

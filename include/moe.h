@@ -25,7 +25,9 @@
  *
  * Conventions
  *   - bf16 tensors are passed as uint16_t bit patterns.
- *   - Packed int4: code 8c+j of a row is bits 4j..4j+3 of uint32 word c.
+ *   - Packed int4: code 8c+j of a row is bits 4j..4j+3 of uint32 word c;
+ *     packed int8 (moe_create_quant with bits = 8): code 4c+j is bits
+ *     8j..8j+7 of word c.
  *   - Every function returns a moe_status (0 = MOE_OK, negative = error);
  *     moe_last_error(ctx) gives a one-line message.  Nothing here throws,
  *     aborts or prints.
@@ -97,6 +99,19 @@ typedef struct moe_weights {
  * E, hidden, inter, shared_inter or group outside those sets; MOE_ERR_CUDA if
  * no device is current. */
 int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out);
+
+/* As moe_create, with the experts' code width `bits` in {4, 8} (the pages'
+ * MLX affine quantisation comes in int4 and int8 widths: README, its list of
+ * what was built).  bits = 4 is moe_create.  With bits = 8 the packed words
+ * of every moe_qmatrix hold 4 codes (code 4c+j of a row is bits 8j..8j+7 of
+ * word c, low byte first), q is uint32 [rows][cols/4], w = s*q + b with q in
+ * [0, 255]; such a context runs the general CUDA-core path for every T (the
+ * decode, batched and grouped-GEMM kernels and stacks are int4 only:
+ * MOE_PATH_DECODE and MOE_PATH_PREFILL return MOE_ERR_UNSUPPORTED and
+ * moe_stack_create refuses it).  Errors: as moe_create, and
+ * MOE_ERR_UNSUPPORTED for another `bits`. */
+int moe_create_quant(int E, int k, int hidden, int inter, int shared_inter, int group, int bits,
+                     moe_ctx** out);
 
 /* Copy and repack the weights into library-owned device memory (on the pages
  * the routed experts sit in a container of equal-stride records, one per

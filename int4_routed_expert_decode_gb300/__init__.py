@@ -39,7 +39,7 @@ EXPORTS = (
     "moe_route_static", "moe_set_test_flags", "moe_set_stage_events", "moe_stack_create",
     "moe_stack_forward", "moe_stack_get_status", "moe_stack_set_test_flags", "moe_stack_destroy",
     "moe_router_check_stats", "moe_pool_enable", "moe_pool_stats", "moe_pool_table",
-    "moe_gdn_recurrence",
+    "moe_gdn_recurrence", "moe_create_quant",
 )
 
 
@@ -78,6 +78,8 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     L.moe_create.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+    L.moe_create_quant.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+    L.moe_create_quant.restype = i32
     L.moe_load_weights.argtypes = [vp, ctypes.POINTER(Weights), i32, vp]
     L.moe_reserve.argtypes = [vp, i32]
     L.moe_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
@@ -169,6 +171,13 @@ def moe_create(E, k, hidden, inter, shared_inter, group) -> int:
     return out.value
 
 
+def moe_create_quant(E, k, hidden, inter, shared_inter, group, bits) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().moe_create_quant(E, k, hidden, inter, shared_inter, group, bits,
+                                  ctypes.byref(out)))
+    return out.value
+
+
 def make_weights(W: dict, on_device: bool) -> tuple[Weights, list]:
     """moe_weights from a dict of canonical arrays (numpy for host, torch for device).
 
@@ -220,12 +229,13 @@ def moe_get_status(ctx: int, stream=None) -> int:
     return lib().moe_get_status(ctx, _stream(stream))
 
 
-def moe_read_expert(ctx: int, slot: int, H: int, I: int, G: int) -> dict:
+def moe_read_expert(ctx: int, slot: int, H: int, I: int, G: int, bits: int = 4) -> dict:
+    c = 32 // bits  # codes per packed word
     out = {
-        "gate_q": np.empty((I, H // 8), np.uint32), "gate_s": np.empty((I, H // G), np.uint16),
-        "gate_b": np.empty((I, H // G), np.uint16), "up_q": np.empty((I, H // 8), np.uint32),
+        "gate_q": np.empty((I, H // c), np.uint32), "gate_s": np.empty((I, H // G), np.uint16),
+        "gate_b": np.empty((I, H // G), np.uint16), "up_q": np.empty((I, H // c), np.uint32),
         "up_s": np.empty((I, H // G), np.uint16), "up_b": np.empty((I, H // G), np.uint16),
-        "down_q": np.empty((H, I // 8), np.uint32), "down_s": np.empty((H, I // G), np.uint16),
+        "down_q": np.empty((H, I // c), np.uint32), "down_s": np.empty((H, I // G), np.uint16),
         "down_b": np.empty((H, I // G), np.uint16),
     }
     order = ("gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q", "down_s", "down_b")
@@ -407,9 +417,10 @@ class MoELayer:
     """
 
     def __init__(self, E, k, H, I, Is, G, weights: dict | None = None, n_slots=None,
-                 max_T=1, on_device=False):
+                 max_T=1, on_device=False, bits=4):
         self.E, self.k, self.H, self.I, self.Is, self.G = E, k, H, I, Is, G
-        self.ctx = moe_create(E, k, H, I, Is, G)
+        self.bits = bits
+        self.ctx = moe_create_quant(E, k, H, I, Is, G, bits)
         if weights is not None:
             self.load(weights, n_slots or E, on_device)
         moe_reserve(self.ctx, max_T)

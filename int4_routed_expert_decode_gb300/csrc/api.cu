@@ -133,11 +133,12 @@ bool qm_ok(const moe_qmatrix& m) { return m.q && m.s && m.b; }
 struct CanonSizes {
   size_t gq, gsb, dq, dsb;  // q words of gate (= up), s (= b) of gate, q of down, s of down
 };
-CanonSizes canon_sizes(int H, int I, int G) {
+CanonSizes canon_sizes(int H, int I, int G, int bits) {
   CanonSizes s;
-  s.gq = (size_t)I * (H / 8) * 4;
+  const int cpw = 32 / bits;  // codes per packed word
+  s.gq = (size_t)I * (H / cpw) * 4;
   s.gsb = (size_t)I * (H / G) * 2;
-  s.dq = (size_t)H * (I / 8) * 4;
+  s.dq = (size_t)H * (I / cpw) * 4;
   s.dsb = (size_t)H * (I / G) * 2;
   return s;
 }
@@ -145,15 +146,15 @@ CanonSizes canon_sizes(int H, int I, int G) {
 // Copy `n` experts starting at index e0 of the canonical arrays (host or
 // device) into blobs[0..n), staging host data through device memory.
 int load_experts(moe_ctx* ctx, const moe_qmatrix& g, const moe_qmatrix& u, const moe_qmatrix& d,
-                 int e0, int n, int on_device, int H, int I, int G, uint8_t* blobs,
+                 int e0, int n, int on_device, int H, int I, int G, int bits, uint8_t* blobs,
                  const BlobLayout& L, cudaStream_t st) {
-  const CanonSizes cs = canon_sizes(H, I, G);
+  const CanonSizes cs = canon_sizes(H, I, G, bits);
   if (on_device) {
     cudaError_t e = launch_repack_expert(
         g.q + (size_t)e0 * cs.gq / 4, g.s + (size_t)e0 * cs.gsb / 2, g.b + (size_t)e0 * cs.gsb / 2,
         u.q + (size_t)e0 * cs.gq / 4, u.s + (size_t)e0 * cs.gsb / 2, u.b + (size_t)e0 * cs.gsb / 2,
         d.q + (size_t)e0 * cs.dq / 4, d.s + (size_t)e0 * cs.dsb / 2, d.b + (size_t)e0 * cs.dsb / 2,
-        n, H, I, G, blobs, L, st);
+        n, H, I, G, bits, blobs, L, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "repack");
     return MOE_OK;
   }
@@ -192,7 +193,8 @@ int load_experts(moe_ctx* ctx, const moe_qmatrix& g, const moe_qmatrix& u, const
     }
     e = launch_repack_expert((uint32_t*)gq, (uint16_t*)gs, (uint16_t*)gb, (uint32_t*)uq,
                              (uint16_t*)us, (uint16_t*)ub, (uint32_t*)dq, (uint16_t*)ds,
-                             (uint16_t*)db, m, H, I, G, blobs + (size_t)s0 * L.stride, L, st);
+                             (uint16_t*)db, m, H, I, G, bits, blobs + (size_t)s0 * L.stride, L,
+                             st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) rc = cuda_fail(ctx, e, "repack");
   }
@@ -230,8 +232,15 @@ const char* moe_status_string(int status) {
 const char* moe_last_error(const moe_ctx* ctx) { return ctx ? ctx->c.msg : g_create_msg; }
 
 int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group, moe_ctx** out) {
+  return moe_create_quant(E, k, hidden, inter, shared_inter, group, 4, out);
+}
+
+int moe_create_quant(int E, int k, int hidden, int inter, int shared_inter, int group, int bits,
+                     moe_ctx** out) {
   if (!out) return set_msg(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
+  if (bits != 4 && bits != 8)
+    return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "bits=%d not in {4, 8}", bits);
   if (E < 1 || E > kMaxE) return set_msg(nullptr, MOE_ERR_UNSUPPORTED, "E=%d not in [1, %d]", E, kMaxE);
   if (k < 1 || k > E || k > kMaxK)
     return set_msg(nullptr, MOE_ERR_INVALID_ARG, "k=%d not in [1, min(E, %d)]", k, kMaxK);
@@ -251,9 +260,9 @@ int moe_create(int E, int k, int hidden, int inter, int shared_inter, int group,
   moe_ctx* ctx = new (std::nothrow) moe_ctx();
   if (!ctx) return set_msg(nullptr, MOE_ERR_OOM, "host allocation failed");
   ctx->c.device = dev;
-  ctx->c.d = Dims{E, k, hidden, inter, shared_inter, group};
-  ctx->c.ex = make_blob_layout(hidden, inter, group);
-  ctx->c.sh = make_blob_layout(hidden, shared_inter, group);
+  ctx->c.d = Dims{E, k, hidden, inter, shared_inter, group, bits};
+  ctx->c.ex = make_blob_layout(hidden, inter, group, bits);
+  ctx->c.sh = make_blob_layout(hidden, shared_inter, group, bits);
   *out = ctx;
   return MOE_OK;
 }
@@ -297,7 +306,7 @@ int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stre
     return cuda_fail(ctx, e, "router copy");
   }
   int rc = load_experts(ctx, w->gate, w->up, w->down, 0, n_slots, w->on_device, d.H, d.I, d.G,
-                        c.pool, c.ex, st);
+                        d.bits, c.pool, c.ex, st);
   if (rc == MOE_OK) {  // the decode kernel's bound constants, kept on the host
     float* tmp = nullptr;
     float hv[2] = {0.f, 0.f};
@@ -312,7 +321,7 @@ int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int n_slots, void* stre
   }
   if (rc == MOE_OK)
     rc = load_experts(ctx, w->shared_gate, w->shared_up, w->shared_down, 0, 1, w->on_device, d.H,
-                      d.Is, d.G, c.shared, c.sh, st);
+                      d.Is, d.G, d.bits, c.shared, c.sh, st);
   if (rc == MOE_OK && (e = cudaStreamSynchronize(st)) != cudaSuccess) rc = cuda_fail(ctx, e, "load");
   if (rc != MOE_OK) {
     free_weights(c);
@@ -555,7 +564,7 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
   const int I = slot < 0 ? c.d.Is : c.d.I;
   const BlobLayout& L = slot < 0 ? c.sh : c.ex;
   const uint8_t* blob = slot < 0 ? c.shared : c.pool + (uint64_t)slot * L.stride;
-  const CanonSizes cs = canon_sizes(c.d.H, I, c.d.G);
+  const CanonSizes cs = canon_sizes(c.d.H, I, c.d.G, c.d.bits);
   const size_t total = 2 * cs.gq + 4 * cs.gsb + cs.dq + 2 * cs.dsb;
   uint8_t* stage = nullptr;
   cudaError_t e = cudaMalloc(&stage, total);
@@ -570,7 +579,7 @@ int moe_read_expert(moe_ctx* ctx, int slot, uint32_t* gate_q, uint16_t* gate_s, 
   uint8_t* ddq = p; p += cs.dq;
   uint8_t* dds = p; p += cs.dsb;
   uint8_t* ddb = p;
-  e = launch_unpack_expert(blob, c.d.H, I, c.d.G, L, (uint32_t*)dgq, (uint16_t*)dgs,
+  e = launch_unpack_expert(blob, c.d.H, I, c.d.G, c.d.bits, L, (uint32_t*)dgq, (uint16_t*)dgs,
                            (uint16_t*)dgb, (uint32_t*)duq, (uint16_t*)dus, (uint16_t*)dub,
                            (uint32_t*)ddq, (uint16_t*)dds, (uint16_t*)ddb, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -1212,7 +1212,8 @@ bool encode_rows(CUtensorMap* m, const uint8_t* base, int row_bytes, int rows, i
 
 bool decode_shape_ok(const Dims& d) {
   const int nj = d.H / 256;
-  return (nj == 1 || nj == 2 || nj == 4 || nj == 8) && d.I == d.Is && d.E <= kMaxE &&
+  return d.bits == 4 && (nj == 1 || nj == 2 || nj == 4 || nj == 8) && d.I == d.Is &&
+         d.E <= kMaxE &&
          d.I % 32 == 0 && d.k <= 32;
 }
 

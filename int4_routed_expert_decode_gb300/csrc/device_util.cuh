@@ -56,6 +56,21 @@ __device__ __forceinline__ float dot_chunk32(uint4 w, const float* __restrict__ 
   return acc;
 }
 
+// The same for 32 int8 codes: word j of a, then of b, holds codes 4j..4j+3
+// (8 bits each, low byte first).
+__device__ __forceinline__ float dot_chunk32_q8(uint4 a, uint4 b, const float* __restrict__ xs) {
+  const uint32_t ws[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      acc = fmaf((float)((ws[j] >> (8 * n)) & 0xFFu), xs[4 * j + n], acc);
+    }
+  }
+  return acc;
+}
+
 // silu(a) = a / (1 + e^-a); the fast division's error (a few ulp of fp32) is
 // far below the bf16 or fp32 rounding of what consumes it.
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }

@@ -1,5 +1,6 @@
-// experts_general.cu -- expert-major int4 GEMV kernels for any T (the
-// general path), plus the deterministic combine.
+// experts_general.cu -- expert-major int4 / int8 GEMV kernels for any T (the
+// general path, and the only one for int8 experts), plus the deterministic
+// combine.
 //
 // For every expert in use (and the shared expert, which takes every token)
 // a CTA streams a tile of the expert's rows and applies it to all of the
@@ -7,8 +8,8 @@
 //   gate/up:  h[q, i] = silu(Wg_i . x_t) * (Wu_i . x_t)         (q = pair position)
 //   down:     o[q, r] = Wd_r . h[q, :]
 //   combine:  y[t, r] = sum_j w[t, j] o[inv[t*k + j], r] + g_t o[P + t, r]
-// with W = s*q + b per group (MLX affine int4; Swiftlet README, its list of
-// what was built).  The affine terms are folded per 32-code
+// with W = s*q + b per group (MLX affine int4 or int8; Swiftlet README, its
+// list of what was built).  The affine terms are folded per 32-code
 // chunk: sum_c (s q_c + b) x_c = s * sum_c q_c x_c + b * sum_c x_c, the last
 // sum staged once per token.
 #include "device_util.cuh"
@@ -78,6 +79,17 @@ __device__ void stage_rows(float* xs, float* xsum, int tc, int K, Loader src) {
   __syncthreads();
 }
 
+// BITS: code width; a 32-code chunk is BITS/4 uint4 words.
+template <int BITS>
+__device__ __forceinline__ float dot_codes(const uint4* chunk, const float* xv) {
+  if constexpr (BITS == 4) {
+    return dot_chunk32(__ldg(chunk), xv);
+  } else {
+    return dot_chunk32_q8(__ldg(chunk), __ldg(chunk + 1), xv);
+  }
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(kWarps * 32) gateup_general_kernel(
     const uint16_t* __restrict__ x, int T, int k, int H, int I, int Is, int G,
     const int32_t* __restrict__ perm, const int32_t* __restrict__ offsets,
@@ -94,7 +106,8 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_general_kernel(
   const BlobLayout& B = U.shared ? LS : L;
   const uint32_t* guq = reinterpret_cast<const uint32_t*>(U.blob + B.gu_q);
   const uint32_t* gusb = reinterpret_cast<const uint32_t*>(U.blob + B.gu_sb);
-  const int nch = H / 32, wrow = H / 8, grow = H / G;
+  constexpr int V = BITS / 4;  // uint4 words per 32-code chunk
+  const int nch = H / 32, wrow = H * BITS / 32, grow = H / G;
   float* xs = smem;
   float* xsum = smem + tcmax * H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -113,7 +126,6 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_general_kernel(
       const uint4* rg = reinterpret_cast<const uint4*>(guq + (size_t)(2 * f) * wrow);
       const uint4* ru = reinterpret_cast<const uint4*>(guq + (size_t)(2 * f + 1) * wrow);
       for (int c = lane; c < nch; c += 32) {
-        const uint4 wg = __ldg(rg + c), wu = __ldg(ru + c);
         const int g = (c * 32) / G;
         const uint32_t sbg = __ldg(gusb + (size_t)(2 * f) * grow + g);
         const uint32_t sbu = __ldg(gusb + (size_t)(2 * f + 1) * grow + g);
@@ -122,8 +134,8 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_general_kernel(
           if (tt < tc) {
             const float* xv = xs + tt * H + c * 32;
             const float xsm = xsum[tt * nch + c];
-            pg[tt] += bf16_lo(sbg) * dot_chunk32(wg, xv) + bf16_hi(sbg) * xsm;
-            pu[tt] += bf16_lo(sbu) * dot_chunk32(wu, xv) + bf16_hi(sbu) * xsm;
+            pg[tt] += bf16_lo(sbg) * dot_codes<BITS>(rg + c * V, xv) + bf16_hi(sbg) * xsm;
+            pu[tt] += bf16_lo(sbu) * dot_codes<BITS>(ru + c * V, xv) + bf16_hi(sbu) * xsm;
           }
         }
       }
@@ -139,6 +151,7 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_general_kernel(
   }
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(kWarps * 32) down_general_kernel(
     int T, int k, int H, int I, int Is, int G, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ used, const int32_t* __restrict__ n_used, const int32_t* table,
@@ -156,7 +169,8 @@ __global__ void __launch_bounds__(kWarps * 32) down_general_kernel(
   const int K = U.inter;
   const uint32_t* dq = reinterpret_cast<const uint32_t*>(U.blob + B.d_q);
   const uint32_t* dsb = reinterpret_cast<const uint32_t*>(U.blob + B.d_sb);
-  const int nch = K / 32, wrow = K / 8, grow = K / G;
+  constexpr int V = BITS / 4;
+  const int nch = K / 32, wrow = K * BITS / 32, grow = K / G;
   float* xs = smem;
   float* xsum = smem + tcmax * K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,12 +186,11 @@ __global__ void __launch_bounds__(kWarps * 32) down_general_kernel(
       for (int tt = 0; tt < kTC; ++tt) pd[tt] = 0.f;
       const uint4* rw = reinterpret_cast<const uint4*>(dq + (size_t)r * wrow);
       for (int c = lane; c < nch; c += 32) {
-        const uint4 w = __ldg(rw + c);
         const uint32_t sb = __ldg(dsb + (size_t)r * grow + (c * 32) / G);
 #pragma unroll
         for (int tt = 0; tt < kTC; ++tt) {
           if (tt < tc) {
-            pd[tt] += bf16_lo(sb) * dot_chunk32(w, xs + tt * K + c * 32) +
+            pd[tt] += bf16_lo(sb) * dot_codes<BITS>(rw + c * V, xs + tt * K + c * 32) +
                       bf16_hi(sb) * xsum[tt * nch + c];
           }
         }
@@ -222,11 +235,13 @@ cudaError_t prepare_general_experts(const Ctx& c) {
   // that preparing one context never lowers the limit under another.
   (void)c;
   const int most = kStageBudget + 1024;
-  cudaError_t e = cudaFuncSetAttribute(gateup_general_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(down_general_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              most);
+  const void* fns[4] = {(const void*)gateup_general_kernel<4>, (const void*)gateup_general_kernel<8>,
+                        (const void*)down_general_kernel<4>, (const void*)down_general_kernel<8>};
+  for (const void* f : fns) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
@@ -239,7 +254,8 @@ cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t 
     const int tc = pick_tc(d.H);
     const size_t smem = (size_t)tc * d.H * 4 + (size_t)tc * (d.H / 32) * 4;
     dim3 grid((maxI + kRowsPerCta - 1) / kRowsPerCta, units);
-    gateup_general_kernel<<<grid, kWarps * 32, smem, st>>>(
+    auto* gk = d.bits == 8 ? gateup_general_kernel<8> : gateup_general_kernel<4>;
+    gk<<<grid, kWarps * 32, smem, st>>>(
         a.x, T, d.k, d.H, d.I, d.Is, d.G, c.ws.perm, c.ws.offsets, c.ws.used, c.ws.n_used,
         a.table, c.n_slots, c.pool, c.ex, c.shared, c.sh, maxI, c.ws.h, tc, c.err);
     ++*launches;
@@ -249,7 +265,8 @@ cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t 
     const int tc = pick_tc(maxI);
     const size_t smem = (size_t)tc * maxI * 4 + (size_t)tc * (maxI / 32) * 4;
     dim3 grid((d.H + kRowsPerCta - 1) / kRowsPerCta, units);
-    down_general_kernel<<<grid, kWarps * 32, smem, st>>>(
+    auto* dk = d.bits == 8 ? down_general_kernel<8> : down_general_kernel<4>;
+    dk<<<grid, kWarps * 32, smem, st>>>(
         T, d.k, d.H, d.I, d.Is, d.G, c.ws.offsets, c.ws.used, c.ws.n_used, a.table, c.n_slots,
         c.pool, c.ex, c.shared, c.sh, maxI, c.ws.h, c.ws.o, tc, c.err);
     ++*launches;

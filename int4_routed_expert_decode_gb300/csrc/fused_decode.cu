@@ -582,7 +582,8 @@ cudaError_t prepare_t(int smem, int* occ) {
 
 bool shape_ok(const Dims& d) {
   const int nj = d.H / 256;
-  return (nj == 1 || nj == 2 || nj == 4 || nj == 8) && d.I == d.Is && d.I <= 1024 &&
+  return d.bits == 4 && (nj == 1 || nj == 2 || nj == 4 || nj == 8) && d.I == d.Is &&
+         d.I <= 1024 &&
          d.E <= kMaxE;
 }
 

@@ -34,10 +34,12 @@ struct BlobLayout {
   uint64_t gu_q, gu_sb, d_q, d_sb, stride;
 };
 
-BlobLayout make_blob_layout(int H, int I, int G);
+// bits: code width (4 or 8), 32/bits codes per packed word.
+BlobLayout make_blob_layout(int H, int I, int G, int bits);
 
 struct Dims {
   int E, k, H, I, Is, G;
+  int bits = 4;  // expert code width: 4 (every path) or 8 (the general path)
 };
 
 // cuTensorMapEncodeTiled, reached through the runtime (null if unavailable).
@@ -163,9 +165,10 @@ struct Ctx {
 cudaError_t launch_repack_expert(const uint32_t* gq, const uint16_t* gs, const uint16_t* gb,
                                  const uint32_t* uq, const uint16_t* us, const uint16_t* ub,
                                  const uint32_t* dq, const uint16_t* ds, const uint16_t* db,
-                                 int n, int H, int I, int G, uint8_t* blobs,
+                                 int n, int H, int I, int G, int bits, uint8_t* blobs,
                                  const BlobLayout& L, cudaStream_t st);
-cudaError_t launch_unpack_expert(const uint8_t* blob, int H, int I, int G, const BlobLayout& L,
+cudaError_t launch_unpack_expert(const uint8_t* blob, int H, int I, int G, int bits,
+                                 const BlobLayout& L,
                                  uint32_t* gq, uint16_t* gs, uint16_t* gb, uint32_t* uq,
                                  uint16_t* us, uint16_t* ub, uint32_t* dq, uint16_t* ds,
                                  uint16_t* db, cudaStream_t st);

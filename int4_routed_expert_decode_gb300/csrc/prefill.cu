@@ -638,7 +638,7 @@ int prefill_max_tiles(const Dims& d, int max_T) {
 }
 
 bool prefill_supported(const Dims& d) {
-  return d.H % kBM == 0 && (2 * d.I) % kBM == 0 && (2 * d.Is) % kBM == 0 && d.I % kBK == 0 &&
+  return d.bits == 4 && d.H % kBM == 0 && (2 * d.I) % kBM == 0 && (2 * d.Is) % kBM == 0 && d.I % kBK == 0 &&
          d.Is % kBK == 0 && d.E <= 1024;
 }
 

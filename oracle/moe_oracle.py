@@ -57,8 +57,8 @@ def f32_to_f64(a) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# MLX affine int4 group quantisation (README: "MLX affine int4/int8 group
-# quantization compute in Metal")
+# MLX affine int4 / int8 group quantisation (Swiftlet README, its list of what
+# was built)
 # ----------------------------------------------------------------------------
 def unpack_int4(words: np.ndarray, cols: int) -> np.ndarray:
     """Codes [rows, cols] from packed words [rows, cols/8].
@@ -72,14 +72,27 @@ def unpack_int4(words: np.ndarray, cols: int) -> np.ndarray:
     return codes.reshape(w.shape[:-1] + (cols,)).astype(np.int64)
 
 
-def dequantize(q: np.ndarray, s: np.ndarray, b: np.ndarray, group: int) -> np.ndarray:
+def unpack_int8(words: np.ndarray, cols: int) -> np.ndarray:
+    """Codes [rows, cols] from packed words [rows, cols/4].
+
+    Reading: code 4c+j of a row sits in bits 8j..8j+7 of word c (low byte
+    first), the same MLX convention at 8 bits per code.
+    """
+    w = np.asarray(words, dtype=np.uint32)
+    shifts = (8 * np.arange(4, dtype=np.uint32))
+    codes = (w[..., None] >> shifts) & np.uint32(0xFF)
+    return codes.reshape(w.shape[:-1] + (cols,)).astype(np.int64)
+
+
+def dequantize(q: np.ndarray, s: np.ndarray, b: np.ndarray, group: int,
+               bits: int = 4) -> np.ndarray:
     """W[r, c] = s[r, c // group] * q[r, c] + b[r, c // group]  (float64).
 
     Reading: groups run along the input (column) dimension; scale and bias are
-    bf16 arrays [rows, cols/group].
+    bf16 arrays [rows, cols/group]; `bits` is the code width (4 or 8).
     """
-    cols = q.shape[-1] * 8
-    codes = unpack_int4(q, cols).astype(np.float64)
+    cols = q.shape[-1] * (32 // bits)
+    codes = (unpack_int4(q, cols) if bits == 4 else unpack_int8(q, cols)).astype(np.float64)
     sc = np.repeat(bf16_to_f64(s), group, axis=-1)
     bi = np.repeat(bf16_to_f64(b), group, axis=-1)
     return sc * codes + bi
@@ -220,11 +233,11 @@ def permutation(topk_idx: np.ndarray, E: int):
 # ----------------------------------------------------------------------------
 # experts and combine
 # ----------------------------------------------------------------------------
-def expert_matrices(ex: dict, i: int, group: int):
+def expert_matrices(ex: dict, i: int, group: int, bits: int = 4):
     """Dequantised (Wg [I,H], Wu [I,H], Wd [H,I]) of expert i of a stacked dict."""
-    Wg = dequantize(ex["gate_q"][i], ex["gate_s"][i], ex["gate_b"][i], group)
-    Wu = dequantize(ex["up_q"][i], ex["up_s"][i], ex["up_b"][i], group)
-    Wd = dequantize(ex["down_q"][i], ex["down_s"][i], ex["down_b"][i], group)
+    Wg = dequantize(ex["gate_q"][i], ex["gate_s"][i], ex["gate_b"][i], group, bits)
+    Wu = dequantize(ex["up_q"][i], ex["up_s"][i], ex["up_b"][i], group, bits)
+    Wd = dequantize(ex["down_q"][i], ex["down_s"][i], ex["down_b"][i], group, bits)
     return Wg, Wu, Wd
 
 
@@ -245,8 +258,9 @@ def moe_block(x_bits: np.ndarray, W: dict, k: int, group: int, tokens=None) -> d
     """The whole block.
 
     ``W``: canonical weights (keys router_w, router_bias, shared_gate_w,
-    shared, experts).  ``tokens``: optional list of token rows for which y is
-    computed (routing and the permutation always cover every token).
+    shared, experts; optional ``bits``, the experts' code width, 4 when
+    absent).  ``tokens``: optional list of token rows for which y is computed
+    (routing and the permutation always cover every token).
 
     Returns a dict with y (float64 [len(tokens), H]), topk_idx, topk_w,
     shared_gate, perm, offsets, logits, tokens.
@@ -254,6 +268,7 @@ def moe_block(x_bits: np.ndarray, W: dict, k: int, group: int, tokens=None) -> d
     x_bits = np.asarray(x_bits)
     T, H = x_bits.shape
     E = W["router_w"].shape[0]
+    bits = int(W.get("bits", 4))
     idx, wts, gate, logits = route(x_bits, W, k)
     perm, offsets = permutation(idx, E)
     toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
@@ -265,12 +280,12 @@ def moe_block(x_bits: np.ndarray, W: dict, k: int, group: int, tokens=None) -> d
             pairs.setdefault(int(idx[t, j]), []).append((r, j))
     o = np.zeros((len(toks), k, H))
     for e, lst in pairs.items():
-        mats = expert_matrices(W["experts"], e, group)
+        mats = expert_matrices(W["experts"], e, group, bits)
         rows = [r for r, _ in lst]
         out = expert_mlp(mats, X[rows])
         for n, (r, j) in enumerate(lst):
             o[r, j] = out[n]
-    shared = expert_mlp(expert_matrices(W["shared"], 0, group), X)
+    shared = expert_mlp(expert_matrices(W["shared"], 0, group, bits), X)
     y = np.zeros((len(toks), H))
     for r, t in enumerate(toks):
         acc = np.zeros(H)

@@ -169,6 +169,32 @@ def layer_weights(seed: int, workload: int, layer: int, shape: Shape,
     }
 
 
+def to_int8_experts(seed: int, workload: int, layer: int, ex: dict, shared: bool) -> dict:
+    """int8 experts of the same sizes drawn from the int4 ones: codes uniform in
+    0..255 (4 per word, fresh streams, tensor ids 37-39), scales s/16 (the int4
+    scale with its bf16 exponent lowered by 4: weights of the same spread) and
+    the int4 biases unchanged (= -128 times the new scale, so code 128 is 0)."""
+    out = {}
+    for i, name in enumerate(("gate", "up", "down")):
+        q4 = ex[name + "_q"]
+        n = q4.size * 2
+        key = stream_key(seed, workload, layer, 37 + i, 1 if shared else 0)
+        out[name + "_q"] = uniform_u32(key, n).reshape(q4.shape[:-1] + (q4.shape[-1] * 2,))
+        out[name + "_s"] = (ex[name + "_s"].astype(np.int32) - (4 << 7)).astype(np.uint16)
+        out[name + "_b"] = ex[name + "_b"].copy()
+    return out
+
+
+def layer_weights_int8(seed: int, workload: int, layer: int, shape: Shape,
+                       zipf_s: float | None = None) -> dict:
+    """As layer_weights, with int8 experts (``bits`` = 8)."""
+    W = layer_weights(seed, workload, layer, shape, zipf_s=zipf_s)
+    W["experts"] = to_int8_experts(seed, workload, layer, W["experts"], False)
+    W["shared"] = to_int8_experts(seed, workload, layer, W["shared"], True)
+    W["bits"] = 8
+    return W
+
+
 T_NORM_W = 30  # tensor id of the stacks' RMSNorm weights (ids below 30 are the C generator's)
 
 

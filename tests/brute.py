@@ -26,10 +26,16 @@ def codes_of_word(word: int) -> list:
     return [int(c, 16) for c in format(int(word), "08x")[::-1]]
 
 
-def dequant_row(qrow, srow, brow, group: int) -> list:
+def codes_of_word8(word: int) -> list:
+    # two hex digits per byte, most-significant byte first; reversed -> byte 0 first
+    h = format(int(word), "08x")
+    return [int(h[i:i + 2], 16) for i in (6, 4, 2, 0)]
+
+
+def dequant_row(qrow, srow, brow, group: int, bits: int = 4) -> list:
     codes = []
     for w in qrow:
-        codes.extend(codes_of_word(w))
+        codes.extend(codes_of_word(w) if bits == 4 else codes_of_word8(w))
     return [bf16(srow[c // group]) * codes[c] + bf16(brow[c // group]) for c in range(len(codes))]
 
 
@@ -43,13 +49,13 @@ def matvec(rows, vec) -> list:
     return out
 
 
-def mlp(ex: dict, i: int, group: int, x: list) -> list:
+def mlp(ex: dict, i: int, group: int, x: list, bits: int = 4) -> list:
     n_in = len(ex["gate_q"][i])
-    gate = [dequant_row(ex["gate_q"][i][r], ex["gate_s"][i][r], ex["gate_b"][i][r], group)
+    gate = [dequant_row(ex["gate_q"][i][r], ex["gate_s"][i][r], ex["gate_b"][i][r], group, bits)
             for r in range(n_in)]
-    up = [dequant_row(ex["up_q"][i][r], ex["up_s"][i][r], ex["up_b"][i][r], group)
+    up = [dequant_row(ex["up_q"][i][r], ex["up_s"][i][r], ex["up_b"][i][r], group, bits)
           for r in range(n_in)]
-    down = [dequant_row(ex["down_q"][i][r], ex["down_s"][i][r], ex["down_b"][i][r], group)
+    down = [dequant_row(ex["down_q"][i][r], ex["down_s"][i][r], ex["down_b"][i][r], group, bits)
             for r in range(len(ex["down_q"][i]))]
     a = matvec(gate, x)
     u = matvec(up, x)
@@ -62,6 +68,7 @@ def block(x_bits, W: dict, k: int, group: int) -> dict:
     T = len(x_bits)
     E = len(W["router_w"])
     rb = W.get("router_bias")
+    bits = W.get("bits", 4)
     ys, idxs, wss, gates = [], [], [], []
     for t in range(T):
         x = [bf16(v) for v in x_bits[t]]
@@ -84,9 +91,9 @@ def block(x_bits, W: dict, k: int, group: int) -> dict:
         g = 1.0 / (1.0 + math.exp(-sum(a * bf16(b) for a, b in zip(x, W["shared_gate_w"]))))
         y = [0.0] * len(x)
         for j, e in enumerate(sel):
-            o = mlp(W["experts"], e, group, x)
+            o = mlp(W["experts"], e, group, x, bits)
             y = [y[h] + w[j] * o[h] for h in range(len(x))]
-        s = mlp(W["shared"], 0, group, x)
+        s = mlp(W["shared"], 0, group, x, bits)
         y = [y[h] + g * s[h] for h in range(len(x))]
         ys.append(y)
         idxs.append(sel)

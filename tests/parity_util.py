@@ -24,7 +24,8 @@ def to_f64_bf16(t) -> np.ndarray:
 
 
 def layer(shape, W, max_T, n_slots=None, device_weights=False):
-    L = moe.MoELayer(shape.E, shape.k, shape.H, shape.I, shape.Is, shape.G, max_T=max_T)
+    L = moe.MoELayer(shape.E, shape.k, shape.H, shape.I, shape.Is, shape.G, max_T=max_T,
+                     bits=int(W.get("bits", 4)))
     if device_weights:
         import torch
         W = to_device(W)

@@ -115,3 +115,12 @@ def test_gdn_recurrence_checks_arguments_before_any_launch(L):
     assert L.moe_gdn_recurrence(None, None, None, None, None, None, None,
                                 1, 1, 2, 4, 128, 8, None) == moe.MOE_ERR_INVALID_ARG
     assert b"NULL" in L.moe_last_error(None)
+
+
+def test_create_quant_checks_bits_before_any_device_call(L):
+    import int4_routed_expert_decode_gb300 as moe
+    out = ctypes.c_void_p()
+    for bits in (0, 2, 3, 5, 16):
+        assert L.moe_create_quant(16, 2, 256, 64, 64, 32, bits, ctypes.byref(out)) == \
+            moe.MOE_ERR_UNSUPPORTED
+        assert b"bits" in L.moe_last_error(None)

@@ -30,12 +30,12 @@ def _unpack_high_first(words, cols):
     return ((w[..., None] >> shifts) & np.uint32(0xF)).reshape(w.shape[:-1] + (cols,)).astype(np.int64)
 
 
-def _dequant_no_bias(q, s, b, group):
+def _dequant_no_bias(q, s, b, group, bits=4):
     codes = O.unpack_int4(q, q.shape[-1] * 8).astype(np.float64)
     return np.repeat(O.bf16_to_f64(s), group, axis=-1) * codes
 
 
-def _dequant_group_off(q, s, b, group):
+def _dequant_group_off(q, s, b, group, bits=4):
     codes = O.unpack_int4(q, q.shape[-1] * 8).astype(np.float64)
     sc = np.tile(O.bf16_to_f64(s), group)  # wrong group index (c % ngroups)
     bi = np.tile(O.bf16_to_f64(b), group)
