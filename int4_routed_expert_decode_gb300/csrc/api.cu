@@ -374,6 +374,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_err = take(4);
   const uint64_t o_bar = take(kSyncWords * 8);
   const uint64_t o_rstats = take(8);
+  const uint64_t o_rcnt = take(16);
   const uint64_t o_tiles = take((uint64_t)prefill_max_tiles(d, max_T) * 16);
   const uint64_t o_ntiles = take(4);
   const uint64_t o_dlayer = take(sizeof(DecLayer));
@@ -406,6 +407,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.err = (int32_t*)(base + o_err);
   c.ws.bar = (unsigned long long*)(base + o_bar);
   c.ws.rstats = (uint32_t*)(base + o_rstats);
+  c.ws.rcnt = (unsigned long long*)(base + o_rcnt);
   c.ws.tiles = base + o_tiles;
   c.ws.n_tiles = (int32_t*)(base + o_ntiles);
   c.dec_layer = (DecLayer*)(base + o_dlayer);
@@ -504,7 +506,10 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
                           c.path == kPathFusedV1)) {
     e = launch_fused_decode(c, a, st, &launches);
   } else {
-    if (use_bdec) {  // logits, exact top-k and the shared gate in two launches
+    if (T <= 64 && small_route_supported(c, T)) {
+      // up to 64 tokens: logits, exact top-k and the shared gate in one launch
+      e = launch_small_route(c, a, st, &launches);
+    } else if (use_bdec) {  // logits, exact top-k and the shared gate in two launches
       e = launch_batch_route(c, a, st, &launches);
     } else {
       e = launch_router(c, a, st, &launches);

@@ -552,8 +552,10 @@ __global__ void __launch_bounds__(256) bdec_router_kernel(
   for (int i = threadIdx.x; i < nrow * (H / 8); i += blockDim.x) {
     const int r = i / (H / 8), j = i - r * (H / 8);
     const uint16_t* src = r < nr ? rw + (size_t)(re0 + r) * H : wsg;
-    rows[i] = __ldg(reinterpret_cast<const uint4*>(src) + j);
+    ptx::cp_async16(rows + i, reinterpret_cast<const uint4*>(src) + j);  // all in flight
   }
+  ptx::cp_async_commit();
+  ptx::cp_async_wait_all();
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int DEPTH = 8 + NJ + 5 + 1;
@@ -640,6 +642,268 @@ __global__ void __launch_bounds__(256) bdec_select_kernel(
   }
 }
 
+// Routing of 2..64 tokens in ONE cooperative launch.
+// Phase 1: CTA c computes the logits of a tile of router rows (one of ES
+// expert slices; slice 0 also the shared-gate row) against a slice of at most
+// kRtTok tokens, both staged in shared memory, with bdec_router_kernel's
+// summation structure (so the same uniform bound per token holds).
+// A bounded grid barrier (a monotonic counter: every launch adds one arrival
+// per CTA), then phase 2: CTA t < T runs the exact top-k of token t.
+constexpr int kRtTok = 16;                     // tokens per token slice
+constexpr uint32_t kRtSpin = 1u << 26;         // barrier polls before giving up
+constexpr uint64_t kRtWaitNs = 1000000000ull;  // ... or one second
+
+template <int NJ>
+__global__ void __launch_bounds__(256, 1) small_route_kernel(
+    const uint16_t* __restrict__ x, int T, const uint16_t* __restrict__ rw,
+    const float* __restrict__ prior, const uint16_t* __restrict__ wsg, int E, int k, float wmax,
+    float pmax, float* __restrict__ logits, float* __restrict__ beta, float* __restrict__ gate_z,
+    unsigned long long* __restrict__ arrive, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, float* __restrict__ gate, int32_t* __restrict__ err) {
+  constexpr int H = NJ * 256, W8 = H / 8;  // 16-byte pieces per row
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  const int nC = gridDim.x, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int TS = (T + kRtTok - 1) / kRtTok, ES = nC / TS;
+  if (c < ES * TS) {
+    // ---- phase 1: the tile (expert slice es, token slice ts)
+    const int ts = c % TS, es = c / TS;
+    const int re0 = (int)(((long long)E * es) / ES), re1 = (int)(((long long)E * (es + 1)) / ES);
+    const int nr = re1 - re0, nrow = nr + (es == 0 ? 1 : 0);
+    const int t0 = ts * kRtTok, nt = min(kRtTok, T - t0);
+    uint4* rows = reinterpret_cast<uint4*>(sm_raw);  // [nrow][W8]
+    uint4* xs = rows + (size_t)nrow * W8;            // [nt][W8]
+    // asynchronous copies: every piece of the tile in flight at once
+    for (int i = threadIdx.x; i < nrow * W8; i += blockDim.x) {
+      const int r = i / W8, j = i - r * W8;
+      const uint16_t* src = r < nr ? rw + (size_t)(re0 + r) * H : wsg;
+      ptx::cp_async16(rows + i, reinterpret_cast<const uint4*>(src) + j);
+    }
+    for (int i = threadIdx.x; i < nt * W8; i += blockDim.x)
+      ptx::cp_async16(xs + i, reinterpret_cast<const uint4*>(x + (size_t)t0 * H) + i);
+    ptx::cp_async_commit();
+    ptx::cp_async_wait_all();
+    __syncthreads();
+    constexpr int DEPTH = 8 + NJ + 5 + 1;
+    // a warp's tokens, each unpacked once into registers and run against
+    // every row of the tile, two rows at a time (two independent sums)
+    for (int i = warp; i < nt; i += blockDim.x >> 5) {
+      float xf[NJ][8];
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const uint4 xv = xs[(size_t)i * W8 + lane + 32 * jj];
+        const uint32_t a4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xf[jj][2 * q] = bf16_lo(a4[q]);
+          xf[jj][2 * q + 1] = bf16_hi(a4[q]);
+        }
+      }
+      for (int r = 0; r < nrow; r += 2) {
+        const int r1 = min(r + 1, nrow - 1);
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) {
+          const uint4 w0 = rows[(size_t)r * W8 + lane + 32 * jj];
+          const uint4 w1 = rows[(size_t)r1 * W8 + lane + 32 * jj];
+          const uint32_t b0[4] = {w0.x, w0.y, w0.z, w0.w}, b1[4] = {w1.x, w1.y, w1.z, w1.w};
+          float sc0 = 0.f, sc1 = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            sc0 = fmaf(xf[jj][2 * q], bf16_lo(b0[q]), sc0);
+            sc0 = fmaf(xf[jj][2 * q + 1], bf16_hi(b0[q]), sc0);
+            sc1 = fmaf(xf[jj][2 * q], bf16_lo(b1[q]), sc1);
+            sc1 = fmaf(xf[jj][2 * q + 1], bf16_hi(b1[q]), sc1);
+          }
+          acc0 += sc0;
+          acc1 += sc1;
+        }
+        acc0 = warp_sum(acc0);
+        acc1 = warp_sum(acc1);
+        if (lane == 0) {
+          for (int h = 0; h < 2 && r + h < nrow; ++h) {
+            const int rr = r + h;
+            const float acc = h ? acc1 : acc0;
+            if (rr < nr)
+              logits[(size_t)(t0 + i) * E + re0 + rr] = acc + (prior ? prior[re0 + rr] : 0.f);
+            else
+              gate_z[t0 + i] = acc;
+          }
+        }
+      }
+      if (es == 0) {  // the token's norm and uniform bound (slice 0 only)
+        float ss = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ss = fmaf(xf[jj][2 * q], xf[jj][2 * q],
+                      fmaf(xf[jj][2 * q + 1], xf[jj][2 * q + 1], ss));
+        ss = warp_sum(ss);
+        const float X = sqrtf(ss * 1.0009765625f) * 1.0009765625f;
+        if (lane == 0)
+          beta[t0 + i] = 2.0f * (float)DEPTH * 5.9604644775390625e-8f * 1.01f * (X * wmax + pmax) +
+                         rt::kBoundFloor;
+      }
+    }
+  }
+  // ---- grid barrier: this CTA's writes, then wait for every CTA's
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned long long old = atomicAdd(arrive, 1ull);
+    const unsigned long long target = (old / (unsigned long long)nC + 1ull) * (unsigned long long)nC;
+    const uint64_t tb = ptx::globaltimer_ns();
+    for (uint32_t it = 0; ptx::ld_acquire_u64(arrive) < target; ++it) {
+      if (it > kRtSpin || ptx::globaltimer_ns() - tb > kRtWaitNs) {
+        record_error(err, MOE_ERR_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (c >= T) return;
+  // ---- phase 2: top-k of token c.  Fast path (as the decode kernel's): an
+  // equal-width histogram of the logits from the top finds the bins holding
+  // the first k + 1 entries; those candidates are ranked by (value, id) and
+  // the order is certified when consecutive values are more than 2 beta apart.
+  // Otherwise the CTA-wide exact routine decides (near-ties, rare).
+  constexpr int V = kMaxE / 256;
+  constexpr int kBinsR = 256, kCapR = 64;
+  const int tid = threadIdx.x;
+  const int need = min(k + 1, E);
+  const float bt = __ldcg(beta + c);  // written by another CTA in this launch: through L2
+  const float* lt = logits + (size_t)c * E;
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm_raw);        // [kBinsR + 1]
+  uint2* s_cand = reinterpret_cast<uint2*>(sm_raw + 2048);       // [kCapR]
+  uint32_t* s_red = reinterpret_cast<uint32_t*>(sm_raw + 2560);  // [16]
+  int* s_sidx = reinterpret_cast<int*>(sm_raw + 2624);           // [33]
+  float* s_sval = reinterpret_cast<float*>(sm_raw + 2768);       // [33]
+  int* s_ok = reinterpret_cast<int*>(sm_raw + 2912);
+  s_hist[tid] = 0u;
+  if (tid == 0) s_hist[kBinsR] = 0u;
+  uint32_t key[V];
+  float lv[V];
+  uint32_t kmx = 0u, kmn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int q = 0; q < V; ++q) {
+    const int e = tid + 256 * q;
+    float f = e < E ? __ldcg(lt + e) : 0.f;
+    if (f != f) f = -INFINITY;
+    lv[q] = f;
+    key[q] = e < E ? rt::f32_key(f) : 0u;
+    if (e < E) {
+      kmx = max(kmx, key[q]);
+      kmn = min(kmn, key[q]);
+    }
+  }
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  kmn = __reduce_min_sync(0xffffffffu, kmn);
+  if (lane == 0) {
+    s_red[warp] = kmx;
+    s_red[8 + warp] = kmn;
+  }
+  __syncthreads();
+  {
+    uint32_t gx = 0u, gn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      gx = max(gx, s_red[w]);
+      gn = min(gn, s_red[8 + w]);
+    }
+    const float M = rt::key_f32(gx), mn = rt::key_f32(gn);
+    const float scale = (M > mn) ? (float)(kBinsR - 1) / (M - mn) : 0.f;
+    int bin[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+      bin[q] = (int)fminf((float)(kBinsR - 1), (M - lv[q]) * scale);
+      if (tid + 256 * q < E) atomicAdd(&s_hist[bin[q]], 1u);
+    }
+    __syncthreads();
+    // smallest bin b* whose cumulative count reaches `need` (every warp)
+    uint32_t cnt[8], run = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cnt[i] = s_hist[8 * lane + i];
+      run += cnt[i];
+    }
+    uint32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, incl >= (uint32_t)need);
+    int bstar = kBinsR - 1;
+    if (hit) {
+      const int hl = __ffs(hit) - 1;
+      uint32_t acc = incl - run;
+      int bl = -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc += cnt[i];
+        if (bl < 0 && acc >= (uint32_t)need) bl = i;
+      }
+      bstar = __shfl_sync(0xffffffffu, 8 * lane + bl, hl);
+    }
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+      const int e = tid + 256 * q;
+      if (e < E && bin[q] <= bstar) {
+        const uint32_t pos = atomicAdd(&s_hist[kBinsR], 1u);
+        if (pos < (uint32_t)kCapR) s_cand[pos] = make_uint2(key[q], (uint32_t)e);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nc = (int)s_hist[kBinsR];
+    bool ok = nc >= need && nc <= kCapR;
+    if (ok) {
+      for (int i = lane; i < nc; i += 32) {
+        const uint2 me = s_cand[i];
+        const uint64_t km = ((uint64_t)me.x << 32) | (uint32_t)~me.y;
+        int rank = 0;
+        for (int j = 0; j < nc; ++j) {
+          const uint2 o = s_cand[j];
+          rank += (((uint64_t)o.x << 32) | (uint32_t)~o.y) > km;
+        }
+        if (rank < need) {
+          s_sidx[rank] = (int)me.y;
+          s_sval[rank] = rt::key_f32(me.x);
+        }
+      }
+      __syncwarp();
+      const bool gap = lane + 1 >= need || (s_sval[lane] - s_sval[lane + 1] > 2.0f * bt);
+      ok = __all_sync(0xffffffffu, gap);
+    }
+    if (lane == 0) *s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  const int* si = s_sidx;
+  const float* sv = s_sval;
+  if (!*s_ok) {
+    __syncthreads();  // every thread has read s_ok before the routine reuses the memory
+    const size_t sel = (rt::topk_warp_smem(E) + 15) & ~size_t(15);
+    int* bi;
+    float* bv;
+    rt::topk_select_block<V>(TokenLogits{lt, bt}, E, k, x + (size_t)c * H, rw, prior, H, sm_raw,
+                             reinterpret_cast<uint2*>(sm_raw + sel),
+                             reinterpret_cast<float*>(sm_raw + sel + 256 * V * 8), &bi, &bv);
+    si = bi;
+    sv = bv;
+  }
+  if (threadIdx.x < 32) {
+    const float w = rt::renormalised_weight(sv, k);
+    if (lane < k) {
+      topk_idx[(size_t)c * k + lane] = si[lane];
+      topk_w[(size_t)c * k + lane] = w;
+    }
+    if (lane == 0) gate[c] = 1.0f / (1.0f + __expf(-__ldcg(gate_z + c)));
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -719,6 +983,14 @@ bool batch_decode_supported(const Ctx& c, int T) {
 }
 
 cudaError_t prepare_batch_decode(const Ctx& c) {
+  {  // the fused small-T routing kernel (any shape it takes)
+    const void* fns[4] = {(const void*)small_route_kernel<1>, (const void*)small_route_kernel<2>,
+                          (const void*)small_route_kernel<4>, (const void*)small_route_kernel<8>};
+    for (const void* f : fns) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmemMax);
+      if (e != cudaSuccess) return e;
+    }
+  }
   BPlan p;
   if (!c.dec_ok || !bplan(c.d, 2, p)) return cudaSuccess;
   cudaError_t e = gu_dispatch(c.d, true, nullptr, 0, nullptr);
@@ -759,6 +1031,56 @@ cudaError_t launch_batch_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, 
                                            c.ws.gate);
   *launches += 2;
   return cudaGetLastError();
+}
+
+namespace {
+// Shared memory of small_route_kernel: phase 1's row and token tiles, or
+// phase 2's selection scratch, whichever is larger.
+size_t small_route_smem(const Dims& d, int T, int nC) {
+  const int TS = (T + kRtTok - 1) / kRtTok, ES = nC / TS;
+  const size_t rows = (size_t)((d.E + ES - 1) / ES + 1);
+  const size_t p1 = (rows + kRtTok) * (size_t)d.H * 2;
+  const size_t p2 = ((rt::topk_warp_smem(d.E) + 15) & ~size_t(15)) + 256 * (kMaxE / 256) * 8 + 64;
+  return p1 > p2 ? p1 : p2;
+}
+
+}  // namespace
+
+bool small_route_supported(const Ctx& c, int T) {
+  return T >= 2 && T <= 64 && c.num_sms >= T && c.num_sms >= (T + kRtTok - 1) / kRtTok &&
+         c.d.H <= 2048 && c.d.H % 256 == 0 && (c.d.H / 256 & (c.d.H / 256 - 1)) == 0 &&
+         c.d.E <= kMaxE && c.ws.rcnt && small_route_smem(c.d, T, c.num_sms) <= kBSmemMax;
+}
+
+cudaError_t launch_small_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches) {
+  const Dims& d = c.d;
+  const int T = f.T;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.num_sms);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = small_route_smem(d, T, c.num_sms);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+#define MOE_SRT(NJ)                                                                            \
+  e = cudaLaunchKernelEx(&cfg, small_route_kernel<NJ>, f.x, T, (const uint16_t*)c.router_w,     \
+                         (const float*)c.router_bias, (const uint16_t*)c.shared_gate_w, d.E,    \
+                         d.k, c.dec_wmax, c.dec_pmax, c.ws.logits, c.ws.bound, c.ws.gate_z,     \
+                         c.ws.rcnt, f.topk_idx, f.topk_w, c.ws.gate, c.err)
+  switch (d.H / 256) {
+    case 1: MOE_SRT(1); break;
+    case 2: MOE_SRT(2); break;
+    case 4: MOE_SRT(4); break;
+    case 8: MOE_SRT(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_SRT
+  ++*launches;
+  return e;
 }
 
 cudaError_t launch_batch_decode(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches) {

@@ -102,6 +102,7 @@ struct Workspace {
   unsigned long long* bar;  // fused kernel: grid-barrier arrival counter (monotonic)
   uint32_t* rstats;   // tensor-core router check: [0] max observed error / (|x| max|Wr|)
                       // (float bits), [1] tokens that fell back to certifying every expert
+  unsigned long long* rcnt;  // small-T routing: grid-barrier arrivals (monotonic)
   void* tiles;        // [max tiles] prefill work tiles (16 bytes each)
   int32_t* n_tiles;   // [1]
 };
@@ -180,6 +181,10 @@ struct FwdArgs;
 bool batch_decode_supported(const Ctx& c, int T);
 cudaError_t prepare_batch_decode(const Ctx& c);
 cudaError_t launch_batch_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches);
+// Routing of 2..64 tokens (logits, exact top-k, weights, shared gate) in one
+// cooperative launch, for hidden <= 2048.
+bool small_route_supported(const Ctx& c, int T);
+cudaError_t launch_small_route(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches);
 cudaError_t launch_batch_decode(const Ctx& c, const FwdArgs& f, cudaStream_t st, int* launches);
 
 struct FwdArgs {
