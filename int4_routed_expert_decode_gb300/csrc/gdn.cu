@@ -203,88 +203,123 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_recurrence_kernel(GdnArgs a) 
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-// ---- T > 1 with the token inputs staged in shared memory ------------------
-// One CTA = 4 warps x 4 rows = 16 consecutive rows of one (sequence, head).
-// The q and k rows of kTC tokens, the CTA's 16 values of v per token and the
-// gates arrive by per-thread asynchronous copies into one of two buffers
-// while the previous chunk is computed; each chunk's norms (|k|^2, |q|^2,
-// k.q) are computed once per CTA, a quarter of the tokens per warp.  The
-// per-token loop then reads shared memory only.  Needs dv % 16 == 0 and
-// 16-byte aligned q, k, v rows.
-constexpr int kSeqRows = 4;                      // rows per warp
-constexpr int kSeqCtaRows = kGdnWarps * kSeqRows;  // 16 rows per CTA
-
+// ---- T > 1: 64 state columns per lane, token inputs staged per chunk -------
+// A row is split over LPR = d_k / 64 lanes (1, 2 or 4), each holding 64 of its
+// columns in registers, so a token's two recalls need log2(LPR) shuffle
+// rounds.  One CTA = 4 warps = RPC consecutive rows of one (sequence, head).
+// Chunks of 16 tokens: q and k (bf16), alpha and beta arrive by asynchronous
+// copies into one of two raw buffers while the previous chunk is computed;
+// then the CTA normalises each token once (a quarter of the tokens per warp)
+// into fp32 k^ and q^ in shared memory, and every lane runs the chunk's
+// tokens against its columns.  v of the next chunk is prefetched into
+// registers.  Needs 16-byte aligned q and k.
 template <int DK>
-struct SeqChunk {
-  static constexpr int kTC = 4096 / DK;  // tokens per chunk: 32 for d_k = 128
-  uint16_t k[kTC][DK];
-  uint16_t q[kTC][DK];
-  uint16_t v[kTC][kSeqCtaRows];
-  float alpha[kTC], beta[kTC];
-  float rk[kTC], rq[kTC], kq[kTC];
+struct SeqGeo {
+  static constexpr int LPR = DK / 64;            // lanes per row
+  static constexpr int RPW = 32 / LPR;           // rows per warp
+  static constexpr int RPC = RPW * kGdnWarps;    // rows per CTA
+  static constexpr int TC = 16;                  // tokens per chunk
+  static constexpr int VPT = TC * RPC / kGdnThreads;  // v values per thread per chunk
+  static constexpr int C = DK / 32;              // columns per lane in the norms pass
 };
 
 template <int DK>
-__device__ __forceinline__ void issue_chunk(const GdnArgs& a, SeqChunk<DK>& c, long b, int h,
-                                            int j, int row0, int t0, int n) {
+struct SeqRaw {  // one buffer of asynchronous copies
+  uint16_t k[SeqGeo<DK>::TC][DK];
+  uint16_t q[SeqGeo<DK>::TC][DK];
+  float alpha[SeqGeo<DK>::TC], beta[SeqGeo<DK>::TC];
+};
+
+template <int DK>
+struct SeqSmem {
+  SeqRaw<DK> raw[2];
+  float kh[SeqGeo<DK>::TC][DK];  // k / sqrt(|k|^2 + eps)
+  float qh[SeqGeo<DK>::TC][DK];  // q / sqrt(|q|^2 + eps) / sqrt(d_k)
+  float kq[SeqGeo<DK>::TC], al[SeqGeo<DK>::TC], be[SeqGeo<DK>::TC];
+  uint16_t v[SeqGeo<DK>::TC][SeqGeo<DK>::RPC];
+};
+
+template <int DK>
+__device__ __forceinline__ void seq_issue(const GdnArgs& a, SeqRaw<DK>& r, long b, int h, int j,
+                                          int t0, int n) {
   constexpr int kSeg = DK * 2 / 16;  // 16-byte pieces of a q or k row
   for (int i = threadIdx.x; i < n * kSeg; i += kGdnThreads) {
     const int t = i / kSeg, p = i - t * kSeg;
     const long off = ((b * a.T + t0 + t) * a.Hk + j) * DK + p * 8;
-    ptx::cp_async16(&c.k[t][p * 8], a.k + off);
-    ptx::cp_async16(&c.q[t][p * 8], a.q + off);
-  }
-  for (int i = threadIdx.x; i < 2 * n; i += kGdnThreads) {
-    const int t = i >> 1, p = i & 1;
-    ptx::cp_async16(&c.v[t][p * 8], a.v + ((b * a.T + t0 + t) * a.Hv + h) * a.dv + row0 + p * 8);
+    ptx::cp_async16(&r.k[t][p * 8], a.k + off);
+    ptx::cp_async16(&r.q[t][p * 8], a.q + off);
   }
   for (int i = threadIdx.x; i < 2 * n; i += kGdnThreads) {
     const int t = i >> 1;
     const long g = (b * a.T + t0 + t) * a.Hv + h;
-    if (i & 1) ptx::cp_async4(&c.beta[t], a.beta + g);
-    else ptx::cp_async4(&c.alpha[t], a.alpha + g);
+    if (i & 1) ptx::cp_async4(&r.beta[t], a.beta + g);
+    else ptx::cp_async4(&r.alpha[t], a.alpha + g);
+  }
+}
+
+template <int DK>
+__device__ __forceinline__ void seq_fetch_v(const GdnArgs& a, long b, int h, int row0, int t0,
+                                            int n, uint16_t (&vr)[SeqGeo<DK>::VPT]) {
+  using P = SeqGeo<DK>;
+#pragma unroll
+  for (int i = 0; i < P::VPT; ++i) {
+    const int idx = threadIdx.x + i * kGdnThreads, t = idx / P::RPC, r = idx - t * P::RPC;
+    vr[i] = (t < n && row0 + r < a.dv) ? a.v[((b * a.T + t0 + t) * a.Hv + h) * a.dv + row0 + r]
+                                       : (uint16_t)0;
   }
 }
 
 template <int DK>
 __global__ void __launch_bounds__(kGdnThreads) gdn_sequence_kernel(GdnArgs a) {
-  constexpr int C = DK / 32;
-  constexpr int R = kSeqRows;
-  constexpr int TC = SeqChunk<DK>::kTC;
+  using P = SeqGeo<DK>;
+  constexpr int TC = P::TC, C = P::C;
   extern __shared__ __align__(16) unsigned char gdn_smem[];
-  SeqChunk<DK>* buf = reinterpret_cast<SeqChunk<DK>*>(gdn_smem);
+  SeqSmem<DK>& S = *reinterpret_cast<SeqSmem<DK>*>(gdn_smem);
 
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ctas_per_head = a.dv / kSeqCtaRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ctas_per_head = (a.dv + P::RPC - 1) / P::RPC;
   const long bh = blockIdx.x / ctas_per_head;
-  const int cta_row0 = static_cast<int>(blockIdx.x - bh * ctas_per_head) * kSeqCtaRows;
+  const int row0 = static_cast<int>(blockIdx.x - bh * ctas_per_head) * P::RPC;
   const int h = static_cast<int>(bh % a.Hv);
   const long b = bh / a.Hv;
   const int j = h / (a.Hv / a.Hk);
-  const int row0 = cta_row0 + warp * R;
-
-  float* srow = a.state + (bh * a.dv + row0) * DK + lane * C;
-  float s[R][C];
+  const int rloc = warp * P::RPW + lane / P::LPR;  // this lane's row within the CTA
+  const int row = row0 + rloc;
+  const bool live = row < a.dv;
+  const int col0 = (lane % P::LPR) * 64;
+  float* srow = a.state + (bh * a.dv + (live ? row : 0)) * DK + col0;
+  float s[64];
 #pragma unroll
-  for (int r = 0; r < R; ++r) load_f32<C>(srow + static_cast<long>(r) * DK, s[r]);
+  for (int c = 0; c < 64; c += 4) {
+    const float4 v4 = live ? *reinterpret_cast<const float4*>(srow + c) : make_float4(0, 0, 0, 0);
+    s[c] = v4.x; s[c + 1] = v4.y; s[c + 2] = v4.z; s[c + 3] = v4.w;
+  }
 
   const int n_chunks = (a.T + TC - 1) / TC;
-  issue_chunk<DK>(a, buf[0], b, h, j, cta_row0, 0, min(TC, a.T));
+  seq_issue<DK>(a, S.raw[0], b, h, j, 0, min(TC, a.T));
   ptx::cp_async_commit();
+  uint16_t vr[P::VPT];
+  seq_fetch_v<DK>(a, b, h, row0, 0, min(TC, a.T), vr);
   for (int ch = 0; ch < n_chunks; ++ch) {
     const int t0 = ch * TC, n = min(TC, a.T - t0);
-    SeqChunk<DK>& c = buf[ch & 1];
     if (ch + 1 < n_chunks)
-      issue_chunk<DK>(a, buf[(ch + 1) & 1], b, h, j, cta_row0, t0 + TC, min(TC, a.T - t0 - TC));
+      seq_issue<DK>(a, S.raw[(ch + 1) & 1], b, h, j, t0 + TC, min(TC, a.T - t0 - TC));
     ptx::cp_async_commit();
     ptx::cp_async_wait<1>();
-    __syncthreads();
+    __syncthreads();  // chunk ch landed; every lane is done with chunk ch - 1
+#pragma unroll
+    for (int i = 0; i < P::VPT; ++i) {
+      const int idx = tid + i * kGdnThreads;
+      S.v[idx / P::RPC][idx % P::RPC] = vr[i];
+    }
+    if (ch + 1 < n_chunks) seq_fetch_v<DK>(a, b, h, row0, t0 + TC, min(TC, a.T - t0 - TC), vr);
+    const SeqRaw<DK>& R = S.raw[ch & 1];
     for (int t = warp; t < n; t += kGdnWarps) {  // the chunk's norms, once per CTA
       float kf[C], qf[C];
-      load_bf16<C>(&c.k[t][lane * C], kf);
-      load_bf16<C>(&c.q[t][lane * C], qf);
+      load_bf16<C>(&R.k[t][lane * C], kf);
+      load_bf16<C>(&R.q[t][lane * C], qf);
       float n3[3] = {0.f, 0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < C; ++e) {
@@ -293,58 +328,72 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_sequence_kernel(GdnArgs a) {
         n3[2] = fmaf(kf[e], qf[e], n3[2]);
       }
       warp_sum<3>(n3);
+      const float rk = 1.0f / sqrtf(n3[0] + a.eps);
+      const float rq = a.inv_sqrt_dk / sqrtf(n3[1] + a.eps);
+#pragma unroll
+      for (int e = 0; e < C; ++e) {
+        S.kh[t][lane * C + e] = __fmul_rn(kf[e], rk);
+        S.qh[t][lane * C + e] = __fmul_rn(qf[e], rq);
+      }
       if (lane == 0) {
-        const float rk = 1.0f / sqrtf(n3[0] + a.eps);
-        const float rq = a.inv_sqrt_dk / sqrtf(n3[1] + a.eps);
-        c.rk[t] = rk;
-        c.rq[t] = rq;
-        c.kq[t] = __fmul_rn(__fmul_rn(n3[2], rk), rq);
+        S.kq[t] = __fmul_rn(__fmul_rn(n3[2], rk), rq);
+        S.al[t] = R.alpha[t];
+        S.be[t] = R.beta[t];
       }
     }
     __syncthreads();
     for (int t = 0; t < n; ++t) {
-      float kf[C], qf[C];
-      load_bf16<C>(&c.k[t][lane * C], kf);
-      load_bf16<C>(&c.q[t][lane * C], qf);
-      float d[2 * R];
+      const float* kh = &S.kh[t][col0];
+      const float* qh = &S.qh[t][col0];
+      float sk[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float sk = 0.f, sq = 0.f;
-#pragma unroll
-        for (int e = 0; e < C; ++e) {
-          sk = fmaf(s[r][e], kf[e], sk);
-          sq = fmaf(s[r][e], qf[e], sq);
-        }
-        d[2 * r] = sk;
-        d[2 * r + 1] = sq;
+      for (int c = 0; c < 64; c += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kh + c);
+        const float4 q4 = *reinterpret_cast<const float4*>(qh + c);
+        const int g = (c >> 2) & 3;
+        sk[g] = fmaf(s[c], k4.x, sk[g]);
+        sk[g] = fmaf(s[c + 1], k4.y, sk[g]);
+        sk[g] = fmaf(s[c + 2], k4.z, sk[g]);
+        sk[g] = fmaf(s[c + 3], k4.w, sk[g]);
+        sq[g] = fmaf(s[c], q4.x, sq[g]);
+        sq[g] = fmaf(s[c + 1], q4.y, sq[g]);
+        sq[g] = fmaf(s[c + 2], q4.z, sq[g]);
+        sq[g] = fmaf(s[c + 3], q4.w, sq[g]);
       }
-      warp_sum<2 * R>(d);
-      const float rk = c.rk[t], rq = c.rq[t], kq = c.kq[t];
-      const float alpha = c.alpha[t], beta = c.beta[t];
-      float kh[C];
+      float dk = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+      float dq = (sq[0] + sq[1]) + (sq[2] + sq[3]);
 #pragma unroll
-      for (int e = 0; e < C; ++e) kh[e] = __fmul_rn(kf[e], rk);
-      float o_mine = 0.f;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float v = __uint_as_float(static_cast<uint32_t>(c.v[t][warp * R + r]) << 16);
-        const float u = __fmul_rn(beta, __fmaf_rn(-alpha, __fmul_rn(d[2 * r], rk), v));
-#pragma unroll
-        for (int e = 0; e < C; ++e) s[r][e] = __fmaf_rn(u, kh[e], __fmul_rn(alpha, s[r][e]));
-        const float o = __fmaf_rn(u, kq, __fmul_rn(alpha, __fmul_rn(d[2 * r + 1], rq)));
-        if (lane == r) o_mine = o;
+      for (int o = 1; o < P::LPR; o <<= 1) {
+        dk += __shfl_xor_sync(0xffffffffu, dk, o);
+        dq += __shfl_xor_sync(0xffffffffu, dq, o);
       }
-      if (lane < R) a.out[((b * a.T + t0 + t) * a.Hv + h) * a.dv + row0 + lane] = o_mine;
+      const float alpha = S.al[t], beta = S.be[t];
+      const float v = __uint_as_float(static_cast<uint32_t>(S.v[t][rloc]) << 16);
+      const float u = __fmul_rn(beta, __fmaf_rn(-alpha, dk, v));
+      const float o = __fmaf_rn(u, S.kq[t], __fmul_rn(alpha, dq));
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kh + c);
+        s[c] = __fmaf_rn(u, k4.x, __fmul_rn(alpha, s[c]));
+        s[c + 1] = __fmaf_rn(u, k4.y, __fmul_rn(alpha, s[c + 1]));
+        s[c + 2] = __fmaf_rn(u, k4.z, __fmul_rn(alpha, s[c + 2]));
+        s[c + 3] = __fmaf_rn(u, k4.w, __fmul_rn(alpha, s[c + 3]));
+      }
+      if (live && (lane % P::LPR) == 0)
+        a.out[((b * a.T + t0 + t) * a.Hv + h) * a.dv + row] = o;
     }
-    __syncthreads();  // every warp is done with this buffer before it is refilled
   }
+  if (live) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) store_f32<C>(srow + static_cast<long>(r) * DK, s[r]);
+    for (int c = 0; c < 64; c += 4)
+      *reinterpret_cast<float4*>(srow + c) = make_float4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+  }
 }
 
 template <int DK>
 cudaError_t launch_seq(const GdnArgs& a, cudaStream_t st) {
-  const size_t smem = 2 * sizeof(SeqChunk<DK>);
+  using P = SeqGeo<DK>;
+  const size_t smem = sizeof(SeqSmem<DK>);
   static bool configured = false;  // the attribute is per function: set once
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gdn_sequence_kernel<DK>,
@@ -354,7 +403,8 @@ cudaError_t launch_seq(const GdnArgs& a, cudaStream_t st) {
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(a.B) * a.Hv * (a.dv / kSeqCtaRows)));
+  const long ctas_per_head = (a.dv + P::RPC - 1) / P::RPC;
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(a.B) * a.Hv * ctas_per_head));
   cfg.blockDim = dim3(kGdnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -383,9 +433,7 @@ cudaError_t launch_r(const GdnArgs& a, cudaStream_t st) {
 
 template <int DK>
 cudaError_t launch_dk(const GdnArgs& a, int R, cudaStream_t st) {
-  if (a.T > 1 && a.dv % kSeqCtaRows == 0 && aligned(a.q, 16) && aligned(a.k, 16) &&
-      aligned(a.v, 16))
-    return launch_seq<DK>(a, st);
+  if (a.T > 1 && aligned(a.q, 16) && aligned(a.k, 16)) return launch_seq<DK>(a, st);
   if (a.T == 1) {
     switch (R) {
       case 8: return launch_r<DK, 8, false>(a, st);
