@@ -54,13 +54,15 @@ namespace {
 using namespace rt;
 using namespace mmag;
 
-constexpr int kThreads = 256;
-constexpr int kWarps = 8;
+constexpr int kThreads = 384;
+constexpr int kWarps = 12;
 constexpr int kBins = 256;      // histogram of the selection filter (one bin per thread)
 constexpr int kCandCap = 64;    // candidates ranked exactly on the fast path
 constexpr uint32_t kSpin = 1u << 24;         // poll rounds of an exchange
 constexpr uint64_t kWaitNs = 1000000000ull;  // every wait gives up after one second
-static_assert(kBins == kThreads, "the histogram is cleared one bin per thread");
+static_assert(kBins <= kThreads, "the histogram is cleared one bin per thread");
+static_assert(kWarps <= 16, "per-warp scratch: four fields of 16 entries");
+constexpr int kRedSs = 0, kRedMx = 16, kRedMn = 32, kRedSq = 48;  // fields of s_red
 constexpr int kMaxTiles = 12;  // gate/up tiles (16 rows) of one CTA
 // mbarriers: 0 prologue A; 1, 2 prologue B (double); then the gate/up tiles; last the down tile
 constexpr int kMbarTile0 = 3;
@@ -302,14 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   const int g4 = lane >> 2, tg = lane & 3;
 
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + a.sm.mbar);
-  float* s_red = reinterpret_cast<float*>(sm + a.sm.misc);            // [32]
-  int* s_idx = reinterpret_cast<int*>(sm + a.sm.misc + 128);          // [32]
-  float* s_w = reinterpret_cast<float*>(sm + a.sm.misc + 256);        // [32]
-  int* s_slot = reinterpret_cast<int*>(sm + a.sm.misc + 384);         // [32]
-  int* s_sidx = reinterpret_cast<int*>(sm + a.sm.misc + 512);         // [33] ranked candidates
-  float* s_sval = reinterpret_cast<float*>(sm + a.sm.misc + 648);     // [33]
-  float* s_g = reinterpret_cast<float*>(sm + a.sm.misc + 784);        // shared gate
-  const uint8_t* s_zero = sm + a.sm.misc + 800;                       // 16 zero bytes
+  float* s_red = reinterpret_cast<float*>(sm + a.sm.misc);            // [64] per-warp fields
+  int* s_idx = reinterpret_cast<int*>(sm + a.sm.misc + 256);          // [32]
+  float* s_w = reinterpret_cast<float*>(sm + a.sm.misc + 384);        // [32]
+  int* s_slot = reinterpret_cast<int*>(sm + a.sm.misc + 512);         // [32]
+  int* s_sidx = reinterpret_cast<int*>(sm + a.sm.misc + 640);         // [33] ranked candidates
+  float* s_sval = reinterpret_cast<float*>(sm + a.sm.misc + 776);     // [33]
+  float* s_g = reinterpret_cast<float*>(sm + a.sm.misc + 912);        // shared gate
+  const uint8_t* s_zero = sm + a.sm.misc + 928;                       // 16 zero bytes
   float* s_part = reinterpret_cast<float*>(sm + a.sm.part);           // router slice sums
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + a.sm.hist);     // [kBins + 1]
   uint2* s_cand = reinterpret_cast<uint2*>(sm + a.sm.cand);           // [kCandCap]
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     for (int i = 0; i < kNumMbar; ++i) ptx::mbar_init(&mbar[i], 1);
     ptx::fence_mbar_init();
   }
-  if (tid < 4) reinterpret_cast<uint32_t*>(sm + a.sm.misc + 800)[tid] = 0u;
+  if (tid < 4) reinterpret_cast<uint32_t*>(sm + a.sm.misc + 928)[tid] = 0u;
   __syncthreads();
   ptx::griddep_launch_dependents();
   if (tid == 0) {
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
     if (table)
       for (int e = tid; e < E; e += kThreads) s_tab[e] = __ldcg(table + e);
-    s_hist[tid] = 0u;  // histogram and candidate count of this layer
+    if (tid < kBins) s_hist[tid] = 0u;  // histogram and candidate count of this layer
     if (tid == 0) s_hist[kBins] = 0u;
     wait_mbar(&mbar[0], par, a.err);         // router rows, norm weight, shared gate/up
     wait_mbar(&mbar[1 + b], pb_par, a.err);  // descriptor, shared down tile
@@ -458,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         }
       }
       ss = warp_sum(ss);
-      if (lane == 0) s_red[warp] = ss;
+      if (lane == 0) s_red[kRedSs + warp] = ss;
       __syncthreads();
-      float tot = s_red[0];
+      float tot = s_red[kRedSs];
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) tot = __fadd_rn(tot, s_red[w]);
+      for (int w = 1; w < kWarps; ++w) tot = __fadd_rn(tot, s_red[kRedSs + w]);
       const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), a.eps)));
       const uint32_t* nw = reinterpret_cast<const uint32_t*>(pa + a.sm.a_nw);
 #pragma unroll
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (e < H / 8 && (e & ((a.G >> 3) - 1)) == 0) s_xg[e >> (lg - 3)] = s8;
       }
       ssq = warp_sum(ssq);
-      if (lane == 0) s_red[24 + warp] = ssq;
+      if (lane == 0) s_red[kRedSq + warp] = ssq;
     }
     if (c == 0 && a.xn_out)  // the block input, for callers that check each layer
       for (int w = tid; w < XW; w += kThreads)
@@ -615,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     kmx = __reduce_max_sync(0xffffffffu, kmx);
     kmn = __reduce_min_sync(0xffffffffu, kmn);
     if (lane == 0) {
-      reinterpret_cast<uint32_t*>(s_red)[8 + warp] = kmx;
-      reinterpret_cast<uint32_t*>(s_red)[16 + warp] = kmn;
+      reinterpret_cast<uint32_t*>(s_red)[kRedMx + warp] = kmx;
+      reinterpret_cast<uint32_t*>(s_red)[kRedMn + warp] = kmn;
     }
     __syncthreads();
     STAMP(7);
@@ -624,8 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
       uint32_t gx = 0u, gn = 0xFFFFFFFFu;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        gx = max(gx, reinterpret_cast<uint32_t*>(s_red)[8 + w]);
-        gn = min(gn, reinterpret_cast<uint32_t*>(s_red)[16 + w]);
+        gx = max(gx, reinterpret_cast<uint32_t*>(s_red)[kRedMx + w]);
+        gn = min(gn, reinterpret_cast<uint32_t*>(s_red)[kRedMn + w]);
       }
       const float M = key_f32(gx), mn = key_f32(gn);
       // bins of equal width over [min, max], bin 0 at the top: a monotone map,
@@ -676,13 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
     __syncthreads();
     STAMP(14);
-    int* s_ok = reinterpret_cast<int*>(sm + a.sm.misc + 816);      // fast path certified
-    float* s_beta = reinterpret_cast<float*>(sm + a.sm.misc + 820);  // the uniform bound
+    int* s_ok = reinterpret_cast<int*>(sm + a.sm.misc + 944);      // fast path certified
+    float* s_beta = reinterpret_cast<float*>(sm + a.sm.misc + 948);  // the uniform bound
     if (warp == 0) {
       const int nc = (int)s_hist[kBins];
       // uniform bound on every logit's rounding error: 2 D u (|x|_2 max_e |Wr_e|_2
       // + max |prior|) (Cauchy-Schwarz on sum |x w|), with 1% to spare
-      float xx = lane < kWarps ? s_red[24 + lane] : 0.f;
+      float xx = lane < kWarps ? s_red[kRedSq + lane] : 0.f;
       xx = warp_sum(xx);
       const float X = sqrtf(xx) * 1.0009765625f;
       const float beta = DecRouter<NJ>::kScale * 1.01f * (X * D.wmax + D.pmax) + kBoundFloor;
@@ -944,10 +946,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
       STAMP(16);
       __syncthreads();
       STAMP(11);
-      // y rows, all threads: thread (m = tid / 16, jl = tid % 16) takes row m's
-      // experts jl, jl + 16, ... (the shared one is j = k), then a fixed
-      // butterfly over the 16 lanes of the row (deterministic)
-      {
+      // y rows, the first 256 threads: thread (m = tid / 16, jl = tid % 16)
+      // takes row m's experts jl, jl + 16, ... (the shared one is j = k), then a
+      // fixed butterfly over the 16 lanes of the row (deterministic)
+      if (tid < 256) {
         const int m = tid >> 4, jl = tid & 15;
         float part = 0.f;
         for (int j = jl; j <= k; j += 16) {
