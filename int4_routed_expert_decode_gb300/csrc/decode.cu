@@ -63,6 +63,7 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // every wait gives up after one se
 static_assert(kBins <= kThreads, "the histogram is cleared one bin per thread");
 static_assert(kWarps <= 16, "per-warp scratch: four fields of 16 entries");
 constexpr int kRedSs = 0, kRedMx = 16, kRedMn = 32, kRedSq = 48;  // fields of s_red
+constexpr int kGuSplitMax = 4;  // k-splits of a gate/up tile (8 measured slower)
 constexpr int kMaxTiles = 12;  // gate/up tiles (16 rows) of one CTA
 // mbarriers: 0 prologue A; 1, 2 prologue B (double); then the gate/up tiles; last the down tile
 constexpr int kMbarTile0 = 3;
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
   // gate/up tasks: k-splits of whole groups and of an even number of chunks
   // (ldmatrix takes two); a down task is one expert's whole row block
   // (measured: fewer, longer down tasks cost less per chunk)
-  const int nsplit_gu = min(4, HC / max(2, 1 << LCPG)), nsplit_d = 1;
+  const int nsplit_gu = min(kGuSplitMax, HC / max(2, 1 << LCPG)), nsplit_d = 1;
   const bool dswz = I / 2 >= 128;
   const int ncbd = dswz ? I / 256 : 1;
   // gate/up tiles: two units of 8 rows, each one TMA box [column block][row][128 B]
@@ -1029,7 +1030,7 @@ bool plan_smem(const Dims& d, int nC, bool chain, DecSmem& s) {
   if (tiles_max > kMaxTiles || rw_max + 1 > kThreads) return false;
   const int S = std::min(8, H / 256);
   const int cpg2 = std::max(2, G / 32);
-  const int nsg = std::min(4, (H / 32) / cpg2), nsd = 1;
+  const int nsg = std::min(kGuSplitMax, (H / 32) / cpg2), nsd = 1;
   if (nsg < 1 || (I / 32) % cpg2 != 0) return false;
   s.mbar = take(kNumMbar * 8, 16);
   s.misc = take(1024, 16);
