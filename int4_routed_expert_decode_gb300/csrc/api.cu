@@ -518,8 +518,10 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, const int32_t* expert_slot_t
     }
     if (e == cudaSuccess && c.pl.slots) e = launch_pool_update(c, a.topk_idx, T * c.d.k, st, &launches);
     record_mark(c, MOE_MARK_ROUTED, st);
-    if (e == cudaSuccess) e = launch_permute(c, a, st, &launches);
-    if (e == cudaSuccess && use_prefill) e = launch_prefill_plan(c, a, st, &launches);
+    bool tiles_built = false;
+    if (e == cudaSuccess) e = launch_permute(c, a, st, &launches, use_prefill, &tiles_built);
+    if (e == cudaSuccess && use_prefill)
+      e = launch_prefill_plan(c, a, st, &launches, tiles_built);
     record_mark(c, MOE_MARK_PERMUTED, st);
     if (e == cudaSuccess)
       e = use_bdec      ? launch_batch_decode(c, a, st, &launches)

@@ -249,7 +249,10 @@ cudaError_t decode_launch(const Dims& d, int nC, const DecLaunch& p, cudaStream_
 bool prefill_supported(const Dims& d);
 int prefill_max_tiles(const Dims& d, int max_T);
 cudaError_t prepare_prefill(const Ctx& c);
-cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+// The grouped GEMMs' tile list (unless the permutation already built it) and
+// a cleared y accumulator.
+cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches,
+                                bool tiles_built);
 cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
 
@@ -263,7 +266,10 @@ cudaError_t launch_router_candidates(const Ctx& c, const FwdArgs& a, cudaStream_
 
 cudaError_t launch_router(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_topk(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
-cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
+// with_tiles: also build the grouped GEMMs' tile list when the one-CTA
+// permutation runs (then *tiles_built is set).
+cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches,
+                           bool with_tiles, bool* tiles_built);
 cudaError_t launch_general_experts(const Ctx& c, const FwdArgs& a, cudaStream_t st,
                                    int* launches);
 

@@ -7,6 +7,7 @@
 // at least one pair in ascending id; the expert kernels walk it.
 #include "device_util.cuh"
 #include "moe_internal.cuh"
+#include "tiles.cuh"
 
 namespace moe {
 
@@ -107,11 +108,20 @@ __device__ void block_stable_scatter(const int32_t* __restrict__ topk_idx, int p
   if (warp < kScatterWarps) warp_stable_scatter(topk_idx, w0, w1, h, perm, inv, perm_out);
 }
 
-// One CTA does everything (used when the pairs fit one block).
+// One CTA does everything (used when the pairs fit one block), and with
+// `tiles` set also the grouped GEMMs' tile list.
+struct TileArgs {
+  Tile* tiles;  // null: no tile list
+  int32_t* n_tiles;
+  const int32_t* table;
+  int n_slots, T, max_tiles;
+  int32_t* err;
+};
+
 __global__ void __launch_bounds__(1024) permute_small_kernel(
     const int32_t* __restrict__ topk_idx, int P, int E, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, int32_t* __restrict__ used,
-    int32_t* __restrict__ n_used, int32_t* perm_out, int32_t* offsets_out) {
+    int32_t* __restrict__ n_used, int32_t* perm_out, int32_t* offsets_out, TileArgs ta) {
   __shared__ int cnt[kMaxE];
   __shared__ int hist[kScatterWarps * kMaxE];
   __shared__ int warp_tot[32];
@@ -137,6 +147,11 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
   }
   __syncthreads();
   block_stable_scatter(topk_idx, 0, P, cnt, E, hist, perm, inv, perm_out);
+  if (ta.tiles) {
+    __syncthreads();  // used, n_used and offsets are in global memory, written above
+    build_tiles_block(used, n_used, offsets, ta.table, ta.n_slots, ta.T, P, ta.tiles, ta.n_tiles,
+                      ta.max_tiles, ta.err, warp_tot);
+  }
 }
 
 // Large P, pass 1: per-block expert counts.
@@ -194,12 +209,20 @@ __global__ void __launch_bounds__(kScatterWarps * 32) permute_scatter_kernel(
 
 }  // namespace
 
-cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches) {
+cudaError_t launch_permute(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches,
+                           bool with_tiles, bool* tiles_built) {
   const int P = a.T * c.d.k, E = c.d.E;
+  *tiles_built = false;
   if (P <= kPairsPerBlock) {
+    TileArgs ta{nullptr, nullptr, nullptr, 0, 0, 0, nullptr};
+    if (with_tiles) {
+      ta = TileArgs{reinterpret_cast<Tile*>(c.ws.tiles), c.ws.n_tiles, a.table, c.n_slots, a.T,
+                    prefill_max_tiles(c.d, a.T), c.err};
+      *tiles_built = true;
+    }
     permute_small_kernel<<<1, 1024, 0, st>>>(a.topk_idx, P, E, c.ws.perm, c.ws.inv,
                                               c.ws.offsets, c.ws.used, c.ws.n_used, a.perm_out,
-                                              a.offsets_out);
+                                              a.offsets_out, ta);
     ++*launches;
     return cudaGetLastError();
   }

@@ -53,13 +53,14 @@
 #include "device_util.cuh"
 #include "moe_internal.cuh"
 #include "sm100_ptx.cuh"
+#include "tiles.cuh"
 
 namespace moe {
 
 namespace {
 
 constexpr int kBM = 128;       // weight rows per unit (UMMA M)
-constexpr int kBN = 128;       // tokens per tile (largest UMMA N used)
+constexpr int kBN = kTileTokens;  // tokens per tile (largest UMMA N used)
 constexpr int kBK = 64;        // K per chunk: one 128-byte swizzle row of bf16
 constexpr int kStages = 8;     // token rows + packed codes + scale/bias words, and a TMEM A tile
 constexpr int kAhead = 3;      // chunks of copies in flight before the loader marks one full
@@ -85,13 +86,6 @@ static_assert(kDqWarps == 8, "two dequantising warps per TMEM lane quarter");
 static_assert(kACol0 + kStages * kACols <= kTmemCols, "TMEM budget");
 static_assert(kAhead < kStages, "the loader must mark a stage full before it needs that stage again");
 static_assert(kBK == 64 && kACols == 32, "the MMA issue loop unrolls 4 K-steps of 16");
-
-struct Tile {
-  int slot;   // expert slot, or -1 for the shared expert
-  int pos0;   // first pair position (routed) or first token (shared)
-  int ntok;   // tokens in the tile, 0 < ntok <= kBN (0: skipped)
-  int hrow0;  // first row of h that the tile owns
-};
 
 struct GemmArgs {
   const uint16_t* x;       // [T][H] bf16
@@ -566,51 +560,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(
     int P, Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int max_tiles,
     int32_t* err) {
   __shared__ int warp_tot[32];
-  const int nu = *n_used;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int cnt = 0, e = -1;
-  if ((int)threadIdx.x < nu) {
-    e = used[threadIdx.x];
-    cnt = (offsets[e + 1] - offsets[e] + kBN - 1) / kBN;
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int nb = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += nb;
-    }
-    warp_tot[lane] = v;
-  }
-  __syncthreads();
-  const int first = (warp ? warp_tot[warp - 1] : 0) + incl - cnt;
-  const int routed = warp_tot[31];
-  if (e >= 0) {
-    const int slot = table ? table[e] : e;
-    const bool bad = slot < 0 || slot >= n_slots;
-    if (bad) record_error(err, MOE_ERR_SLOT);
-    const int p0 = offsets[e], n_e = offsets[e + 1] - p0;
-    for (int i = 0; i < cnt; ++i) {
-      const int id = first + i;
-      if (id < max_tiles)
-        tiles[id] = Tile{bad ? 0 : slot, p0 + i * kBN, bad ? 0 : min(kBN, n_e - i * kBN),
-                         p0 + i * kBN};
-    }
-  }
-  const int nsh = (T + kBN - 1) / kBN;
-  for (int i = threadIdx.x; i < nsh; i += blockDim.x) {
-    const int id = routed + i;
-    if (id < max_tiles) tiles[id] = Tile{-1, i * kBN, min(kBN, T - i * kBN), P + i * kBN};
-  }
-  if (threadIdx.x == 0) *n_tiles = min(max_tiles, routed + nsh);
+  build_tiles_block(used, n_used, offsets, table, n_slots, T, P, tiles, n_tiles, max_tiles, err,
+                    warp_tot);
 }
 
 // y = bf16(y_acc), four elements per thread step
@@ -654,13 +605,15 @@ cudaError_t prepare_prefill(const Ctx& c) {
 // The tile list of the grouped GEMMs (after the permutation) and a zeroed
 // fp32 accumulator for y.
 cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& fa, cudaStream_t st,
-                                int* launches) {
+                                int* launches, bool tiles_built) {
   const Dims& d = c.d;
   const int T = fa.T, P = T * d.k;
-  build_tiles_kernel<<<1, 1024, 0, st>>>(c.ws.used, c.ws.n_used, c.ws.offsets, fa.table,
-                                         c.n_slots, T, P, reinterpret_cast<Tile*>(c.ws.tiles),
-                                         c.ws.n_tiles, prefill_max_tiles(d, T), c.err);
-  ++*launches;
+  if (!tiles_built) {
+    build_tiles_kernel<<<1, 1024, 0, st>>>(c.ws.used, c.ws.n_used, c.ws.offsets, fa.table,
+                                           c.n_slots, T, P, reinterpret_cast<Tile*>(c.ws.tiles),
+                                           c.ws.n_tiles, prefill_max_tiles(d, T), c.err);
+    ++*launches;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return cudaMemsetAsync(c.ws.o, 0, (size_t)T * d.H * 4, st);
