@@ -102,6 +102,7 @@ struct GemmArgs {
   float* y_acc;            // [T][H] fp32 (zero on entry to the down GEMM)
   int32_t* err;
   int k, H, I, Is, G, hstride, nm;  // nm: weight-row tiles per token tile
+  int64_t yacc_n4;  // gate/up only: float4s of y_acc it clears for the down GEMM
   int test_stall;  // MOE_TEST_WAIT_TIMEOUT: the MMA issuer first waits on a phase nothing completes
 };
 
@@ -241,8 +242,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_units = *a.n_tiles * a.nm;
 
+  // Launched as a programmatic dependent: the prologue below (barriers, TMEM,
+  // the clear of y_acc that no earlier kernel of the call uses) may overlap
+  // the previous kernel; everything it produced is read after griddep_wait.
+  if (!DOWN) {
+    float4* y4 = reinterpret_cast<float4*>(a.y_acc);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a.yacc_n4;
+         i += (int64_t)gridDim.x * blockDim.x)
+      y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&S.raw_full[s], kLoadWarps * 32 + 1);  // loader lanes + the expect-tx arrival
@@ -265,7 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const uint32_t tmem = S.tmem_base;
+  const int n_units = *a.n_tiles * a.nm;
   // scale/bias windows: up to kSbWin group words per row, i.e. cpw chunks
   const int cpw = kSbWin * a.G / kBK;
   const int lg = 31 - __clz(a.G);  // log2 of the group size (32, 64 or 128)
@@ -567,6 +579,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(
 // y = bf16(y_acc), four elements per thread step
 __global__ void finalize_kernel(const float* __restrict__ y_acc, uint16_t* __restrict__ y,
                                 int64_t n4) {
+  ptx::griddep_wait();  // a programmatic dependent of the down GEMM
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 v = reinterpret_cast<const float4*>(y_acc)[i];
@@ -614,9 +627,8 @@ cudaError_t launch_prefill_plan(const Ctx& c, const FwdArgs& fa, cudaStream_t st
                                            c.ws.n_tiles, prefill_max_tiles(d, T), c.err);
     ++*launches;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return cudaMemsetAsync(c.ws.o, 0, (size_t)T * d.H * 4, st);
+  // (y_acc is cleared by the gate/up GEMM's prologue)
+  return cudaGetLastError();
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point, so that
@@ -690,13 +702,34 @@ cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t
   a.hstride = hstride;
   a.nm = 2 * hstride / kBM;
   a.test_stall = (c.test_flags & MOE_TEST_WAIT_TIMEOUT) ? 1 : 0;
-  grouped_gemm_kernel<false><<<c.num_sms, kThreads, kGemmSmem, st>>>(a, gq, gq_sh);
+  a.yacc_n4 = (int64_t)T * d.H / 4;
+  // programmatic dependent launches: each kernel's prologue overlaps the
+  // previous kernel, and griddepcontrol.wait orders every dependent read
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false>, a, gq, gq_sh);
+  if (e != cudaSuccess) return e;
   record_mark(c, MOE_MARK_GATEUP, st);
   a.nm = d.H / kBM;
-  grouped_gemm_kernel<true><<<c.num_sms, kThreads, kGemmSmem, st>>>(a, dq, dq_sh);
+  a.yacc_n4 = 0;
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, a, dq, dq_sh);
+  if (e != cudaSuccess) return e;
   record_mark(c, MOE_MARK_DOWN, st);
   const int64_t n4 = (int64_t)T * d.H / 4;
-  finalize_kernel<<<4 * c.num_sms, 256, 0, st>>>(c.ws.o, fa.y, n4);
+  cudaLaunchConfig_t fcfg = cfg;
+  fcfg.gridDim = dim3(4 * c.num_sms);
+  fcfg.blockDim = dim3(256);
+  fcfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&fcfg, finalize_kernel, (const float*)c.ws.o, fa.y, n4);
+  if (e != cudaSuccess) return e;
   *launches += 3;
   return cudaGetLastError();
 }
