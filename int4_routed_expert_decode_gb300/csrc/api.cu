@@ -375,6 +375,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   const uint64_t o_bar = take(kSyncWords * 8);
   const uint64_t o_rstats = take(8);
   const uint64_t o_rcnt = take(16);
+  const uint64_t o_rovf = take(router_tc_overflow_bytes(d, max_T) + 16);
   const uint64_t o_tiles = take((uint64_t)prefill_max_tiles(d, max_T) * 16);
   const uint64_t o_ntiles = take(4);
   const uint64_t o_dlayer = take(sizeof(DecLayer));
@@ -408,6 +409,7 @@ int moe_reserve(moe_ctx* ctx, int max_T) {
   c.ws.bar = (unsigned long long*)(base + o_bar);
   c.ws.rstats = (uint32_t*)(base + o_rstats);
   c.ws.rcnt = (unsigned long long*)(base + o_rcnt);
+  c.ws.rovf = base + o_rovf;
   c.ws.tiles = base + o_tiles;
   c.ws.n_tiles = (int32_t*)(base + o_ntiles);
   c.dec_layer = (DecLayer*)(base + o_dlayer);

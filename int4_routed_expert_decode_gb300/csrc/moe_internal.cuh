@@ -103,6 +103,7 @@ struct Workspace {
   uint32_t* rstats;   // tensor-core router check: [0] max observed error / (|x| max|Wr|)
                       // (float bits), [1] tokens that fell back to certifying every expert
   unsigned long long* rcnt;  // small-T routing: grid-barrier arrivals (monotonic)
+  uint8_t* rovf;      // tensor-core router: per-token overflow of the candidate selection
   void* tiles;        // [max tiles] prefill work tiles (16 bytes each)
   int32_t* n_tiles;   // [1]
 };
@@ -259,6 +260,9 @@ cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& a, cudaStream_t 
 // Router for many tokens: approximate logits on the tensor cores, then
 // certified logits of each token's candidates and the exact selection.
 bool router_tc_supported(const Dims& d, int T);
+// Workspace bytes for the candidate selection's per-token overflow (0 when the
+// router is never used for up to max_T tokens).
+size_t router_tc_overflow_bytes(const Dims& d, int max_T);
 cudaError_t prepare_router_tc();
 cudaError_t launch_router_tc(const Ctx& c, const FwdArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_router_candidates(const Ctx& c, const FwdArgs& a, cudaStream_t st,

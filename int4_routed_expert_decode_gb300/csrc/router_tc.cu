@@ -42,6 +42,17 @@ constexpr int kRThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
 constexpr int kRTile = kRM * kRK * 2;  // 16 KiB (A and B alike)
 constexpr uint64_t kRWaitNs = 1000000000ull;
 constexpr int kCandWarps = 4;
+constexpr int kCandCap = 64;  // candidates kept in shared memory per token
+// one token's overflow scratch: the selection scratch for E entries, then E
+// candidate ids, logits and bounds
+__host__ __device__ constexpr size_t cand_ovf_bytes(int E) {
+  return (topk_warp_smem(E) + (size_t)E * 12 + 15) & ~size_t(15);
+}
+// per warp: the selection scratch for kCandCap entries, then the candidate
+// ids, logits and bounds
+__host__ __device__ constexpr size_t cand_warp_smem() {
+  return (topk_warp_smem(kCandCap) + (size_t)kCandCap * 12 + 15) & ~size_t(15);
+}
 
 struct RSmem {
   uint8_t a[kRStages][kRTile];
@@ -210,15 +221,27 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
     const float* __restrict__ wnorm, const float* __restrict__ gate_z,
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ router_w,
     const float* __restrict__ prior, int T, int E, int H, int k, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, float* __restrict__ gate, uint32_t* __restrict__ rstats) {
+    float* __restrict__ topk_w, float* __restrict__ gate, uint32_t* __restrict__ rstats,
+    uint8_t* __restrict__ ovf) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kCandWarps + warp;
   if (t >= T) return;
-  uint8_t* ws = smem_raw + (size_t)warp * (topk_warp_smem(E) + (size_t)E * 12);
-  int* cid = reinterpret_cast<int*>(ws + topk_warp_smem(E));
-  float* cl = reinterpret_cast<float*>(cid + E);
-  float* cb = cl + E;
+  // Candidate arrays and selection scratch: in shared memory for up to
+  // kCandCap candidates (the usual case), else in this token's slice of the
+  // global overflow region (E entries: many candidates, or every expert).
+  uint8_t* ws = smem_raw + (size_t)warp * cand_warp_smem();
+  int* cid = reinterpret_cast<int*>(ws + topk_warp_smem(kCandCap));
+  float* cl = reinterpret_cast<float*>(cid + kCandCap);
+  float* cb = cl + kCandCap;
+  bool in_global = false;
+  auto to_global = [&]() {
+    ws = ovf + (size_t)t * cand_ovf_bytes(E);
+    cid = reinterpret_cast<int*>(ws + topk_warp_smem(E));
+    cl = reinterpret_cast<float*>(cid + E);
+    cb = cl + E;
+    in_global = true;
+  };
   const float* arow = approx + (size_t)t * E;
   // the k-th largest approximate logit (entries in lane-major order)
   uint32_t key[MAXV];
@@ -266,8 +289,13 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
   const float xn = __ldg(xnorm + t);
   const float d = 0.0009765625f * xn * wmax + 2.384185791015625e-07f * pmax;
   const float cut = key_f32(kth) - 2.0f * d;
-  // candidates, in expert order
+  // candidates, in expert order (counted first to choose their storage)
   int n = 0;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i)
+    n += __popc(__ballot_sync(0xffffffffu, key[i] != 0u && key_f32(key[i]) >= cut));
+  if (n > kCandCap) to_global();
+  n = 0;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     // lane-major entries: expert lane * MAXV + i; gather per i in lane order,
@@ -311,6 +339,7 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
     if (fallback) atomicAdd(rstats + 1, 1u);
   }
   if (fallback) {
+    if (!in_global) to_global();
     n = E;
     for (int e = lane; e < E; e += 32) cid[e] = e;
     __syncwarp();
@@ -318,9 +347,12 @@ __global__ void __launch_bounds__(kCandWarps * 32) router_candidates_kernel(
   }
   int* sel_idx;
   float* sel_val;
-  // one candidate per lane when they fit (the usual case), else MAXV per lane
+  // one candidate per lane when they fit (the usual case), else two or MAXV
   if (n <= 32)
     topk_select_warp_src<1>(CandLogits{cid, cl, cb}, n, k, x + (size_t)t * H, router_w, prior, H,
+                            ws, &sel_idx, &sel_val);
+  else if (n <= 64)
+    topk_select_warp_src<2>(CandLogits{cid, cl, cb}, n, k, x + (size_t)t * H, router_w, prior, H,
                             ws, &sel_idx, &sel_val);
   else
     topk_select_warp_src<MAXV>(CandLogits{cid, cl, cb}, n, k, x + (size_t)t * H, router_w, prior,
@@ -367,9 +399,13 @@ bool encode_rows128(CUtensorMap* m, const uint16_t* base, int rows, int H) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t cand_smem(int E) { return (size_t)kCandWarps * (topk_warp_smem(E) + (size_t)E * 12); }
+size_t cand_smem() { return (size_t)kCandWarps * cand_warp_smem(); }
 
 }  // namespace
+
+size_t router_tc_overflow_bytes(const Dims& d, int max_T) {
+  return router_tc_supported(d, max_T) ? (size_t)max_T * cand_ovf_bytes(d.E) : 0;
+}
 
 bool router_tc_supported(const Dims& d, int T) {
   return T >= 128 && d.E >= 128 && d.E % 128 == 0 && d.E <= kMaxE && d.H % kRK == 0;
@@ -378,7 +414,7 @@ bool router_tc_supported(const Dims& d, int T) {
 cudaError_t prepare_router_tc() {
   cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kRSmem);
-  const int cs = (int)cand_smem(kMaxE);
+  const int cs = (int)cand_smem();
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(router_candidates_kernel<4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, cs);
@@ -412,11 +448,11 @@ cudaError_t launch_router_candidates(const Ctx& c, const FwdArgs& a, cudaStream_
                                      int* launches) {
   const Dims& d = c.d;
   const int grid = (a.T + kCandWarps - 1) / kCandWarps;
-  const size_t smem = cand_smem(d.E);
+  const size_t smem = cand_smem();
 #define MOE_CAND(MV)                                                                            \
   router_candidates_kernel<MV><<<grid, kCandWarps * 32, smem, st>>>(                           \
       c.ws.logits, c.ws.xnorm, c.ws.wnorm, c.ws.gate_z, a.x, c.router_w, c.router_bias, a.T,    \
-      d.E, d.H, d.k, a.topk_idx, a.topk_w, c.ws.gate, c.ws.rstats)
+      d.E, d.H, d.k, a.topk_idx, a.topk_w, c.ws.gate, c.ws.rstats, c.ws.rovf)
   if (d.E <= 128) MOE_CAND(4);
   else if (d.E <= 256) MOE_CAND(8);
   else if (d.E <= 512) MOE_CAND(16);
