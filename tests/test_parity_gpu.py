@@ -342,6 +342,26 @@ def test_fused_decode_near_ties_across_partial_lists():
         U.assert_parity(out, O.moe_block(x, W, shape.k, shape.G), what=f"partial lists step{step}")
 
 
+@pytest.mark.parametrize("wid", [0, 2])
+def test_decode_far_outlier_logit(wid):
+    """A prior lifts one expert's logit far above the rest: the selection
+    filter's counted bins (the top quarter of [min, max]) then hold fewer than
+    k + 1 logits, every logit becomes a candidate, and the exact routine ranks
+    them; the top-k stays exact and the outlier comes first."""
+    wl = synth.WORKLOADS[wid]
+    W = _weights(wl, layer=4)
+    bias = np.zeros(wl.E, np.float32) if W.get("router_bias") is None else W["router_bias"].copy()
+    bias[5] += 1000.0
+    W["router_bias"] = bias
+    L = U.layer(wl.shape, W, max_T=1)
+    moe.moe_set_path(L.ctx, moe.MOE_PATH_DECODE)
+    for step in range(3):
+        x = _x(wl, 1, layer=4, step=step)
+        out = U.run(L, x)
+        assert out["topk_idx"][0][0] == 5
+        U.assert_parity(out, O.moe_block(x, W, wl.k, wl.G), what=f"outlier wl{wid} step{step}")
+
+
 def test_fused_decode_placement_invariance():
     wl = synth.WORKLOADS[1]
     W = _weights(wl, layer=2)
