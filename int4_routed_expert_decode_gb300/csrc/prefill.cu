@@ -104,6 +104,7 @@ struct GemmArgs {
   int k, H, I, Is, G, hstride, nm;  // nm: weight-row tiles per token tile
   int64_t yacc_n4;  // gate/up only: float4s of y_acc it clears for the down GEMM
   int test_stall;  // MOE_TEST_WAIT_TIMEOUT: the MMA issuer first waits on a phase nothing completes
+  int b_tma;       // bmap is valid: tiles whose token rows are contiguous load B by TMA
 };
 
 struct Smem {
@@ -234,11 +235,15 @@ struct Walk {
 };
 
 // cmap / cmap_sh: the packed codes of the routed pool / the shared blob,
-// 3-D uint32 {K/8, rows, blobs}, box 8 x 128 x 1.
+// 3-D uint32 {K/8, rows, blobs}, box 8 x 128 x 1.  bmap: the B rows (x for
+// gate/up, h for down) as 2-D bf16 {K, rows}, box 64 x kBN, 128-byte swizzle:
+// a tile whose token rows are consecutive (every down tile, the shared
+// expert's gate/up tiles) takes its B tile as one copy per chunk.
 template <bool DOWN>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap cmap,
-                        const __grid_constant__ CUtensorMap cmap_sh) {
+                        const __grid_constant__ CUtensorMap cmap_sh,
+                        const __grid_constant__ CUtensorMap bmap) {
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -340,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int lsb = 0, crow = 0, cblob = 0;
     int rid[4] = {-1, -1, -1, -1};  // token-row ids of this lane's rows (-1: past the tile)
     const CUtensorMap* cm = &cmap;
+    bool btma = false;  // this unit's B tile by TMA, from row brow0
+    int brow0 = 0;
     uint32_t g = 0, done = 0, gw = 0;  // chunks issued, chunks marked full, windows issued
     uint32_t win_start[2] = {0, 0};    // first chunk of the last two windows
     bool ok = true;
@@ -362,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cm = sh ? &cmap_sh : &cmap;
         cblob = sh ? 0 : t.slot;
         crow = w.m0;
+        btma = a.b_tma && (DOWN || sh);
+        brow0 = DOWN ? t.hrow0 : t.pos0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int n = 4 * (lw + kLoadWarps * i) + (lane >> 3);
@@ -402,16 +411,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = S.raw[s];
           if (lt == 0) {
-            ptx::mbar_arrive_expect_tx(&S.raw_full[s], kCodesBytes);
+            // the whole box lands, rows past the tile included (zeros past
+            // the matrix; other tiles' rows otherwise: their columns of D
+            // are never read)
+            ptx::mbar_arrive_expect_tx(&S.raw_full[s], kCodesBytes + (btma ? kTileBytes : 0));
             ptx::tma_load_3d(st + kCodesOff, cm, c * 8, crow, cblob, &S.raw_full[s]);
+            if (btma) ptx::tma_load_2d(st, &bmap, c * kBK, brow0, &S.raw_full[s]);
           }
-          // token rows: piece ch of rows 4 (lw + 8 i) + lane / 8
-          const uint16_t* bsrc = bbase + c * kBK + ch * 8;
+          if (!btma) {
+            // token rows: piece ch of rows 4 (lw + 8 i) + lane / 8
+            const uint16_t* bsrc = bbase + c * kBK + ch * 8;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (rid[i] >= 0)
-              ptx::cp_async16(st + sw128_off(4 * (lw + kLoadWarps * i) + (lane >> 3), ch),
-                              bsrc + (size_t)rid[i] * bpitch);
+            for (int i = 0; i < 4; ++i) {
+              if (rid[i] >= 0)
+                ptx::cp_async16(st + sw128_off(4 * (lw + kLoadWarps * i) + (lane >> 3), ch),
+                                bsrc + (size_t)rid[i] * bpitch);
+            }
           }
           ptx::cp_async_commit();
           ++g;
@@ -666,6 +681,22 @@ bool encode_codes(CUtensorMap* m, const uint8_t* region, int K, int rows, int bl
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of a bf16 matrix (row pitch `pitch` elements) as B tiles: 2-D {cols,
+// rows}, box 64 x kBN, the 128-byte swizzle of the MMA's B descriptor.
+bool encode_rows(CUtensorMap* m, const uint16_t* base, int cols, int rows, int pitch) {
+  if (((uintptr_t)base & 15) != 0 || rows <= 0 || (pitch * 2) % 16 != 0) return false;
+  const cuuint64_t dim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t stride[1] = {(cuuint64_t)pitch * 2};
+  const cuuint32_t box[2] = {kBK, kBN};
+  const cuuint32_t es[2] = {1, 1};
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dim, stride,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t st,
@@ -715,12 +746,19 @@ cudaError_t launch_prefill_experts(const Ctx& c, const FwdArgs& fa, cudaStream_t
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false>, a, gq, gq_sh);
+  // B by TMA where a tile's rows are consecutive: x rows for the shared
+  // expert's gate/up tiles, h rows for every down tile (else per-lane copies)
+  CUtensorMap xmap{}, hmap{};
+  const bool x_tma = encode_rows(&xmap, reinterpret_cast<const uint16_t*>(fa.x), d.H, T, d.H);
+  const bool h_tma = encode_rows(&hmap, a.h, hstride, T * d.k + T, hstride);
+  a.b_tma = x_tma ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false>, a, gq, gq_sh, xmap);
   if (e != cudaSuccess) return e;
   record_mark(c, MOE_MARK_GATEUP, st);
   a.nm = d.H / kBM;
   a.yacc_n4 = 0;
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, a, dq, dq_sh);
+  a.b_tma = h_tma ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, a, dq, dq_sh, hmap);
   if (e != cudaSuccess) return e;
   record_mark(c, MOE_MARK_DOWN, st);
   const int64_t n4 = (int64_t)T * d.H / 4;
