@@ -184,6 +184,8 @@ __device__ void tight_logit_group8(const uint16_t* __restrict__ x,
   if (e >= 0) {
     const uint4* xr = reinterpret_cast<const uint4*>(x);
     const uint4* wr = reinterpret_cast<const uint4*>(router_w + (size_t)e * H);
+    // the loads of several chunks in flight at once (the sums keep their order)
+#pragma unroll 8
     for (int j = 0; j < H / 64; ++j) {
       const uint4 xv = __ldg(xr + sub + 8 * j);
       const uint4 wv = __ldg(wr + sub + 8 * j);
